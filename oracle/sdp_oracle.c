@@ -1,0 +1,258 @@
+/*
+ * Oracle for the fused grouped-query scaled-dot-product attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the slow, obviously correct CPU
+ * definition that the CUDA path is checked against. Only the test suite,
+ * the smoke check and the benchmark's CPU-baseline leg may load it. It shares
+ * no code, header, table or constant with the CUDA library and includes none
+ * of its files.
+ *
+ * What it computes (plain definition, fp64 throughout). For batch b, query
+ * head h and query row i:
+ *
+ *   g        = h / (Hq / Hkv)            grouped-query head mapping: each KV head
+ *                                        serves Hq/Hkv consecutive query heads
+ *                                        ("xe2-sdp-hd256" page, header: 32 Q heads
+ *                                        over 2 KV heads; "SyclKittens" summary,
+ *                                        section E.1: the grouped baseline repeats
+ *                                        each KV head)
+ *   s_j      = scale * sum_d Q[b,h,i,d] * K[b,g,j,d]          for 0 <= j < Skv
+ *   M        = max_j s_j
+ *   L        = sum_j exp(s_j - M)
+ *   O[b,h,i] = sum_j exp(s_j - M) * V[b,g,j,:] / L
+ *   LSE      = M + ln L                  natural log, one value per (b,h,i)
+ *
+ * This is the result the single-pass online-softmax kernel of the
+ * "xe2-sdp-hd256" page (section "HD=256 Architecture Differences") and the
+ * "xe2-sdp-bf16" page (section "Data flow diagram") reaches up to rounding
+ * order. The oracle does not block, fuse or reorder: it forms each score
+ * row in full, then its maximum, then the exponentials, then the weighted
+ * sum of V rows.
+ *
+ * Inputs are the exact 16-bit patterns the GPU receives (fp16 or bf16),
+ * decoded here to double ("xe2-sdp-bf16" page, section "CPU reference must
+ * match input type": the reference consumes the type-quantised values).
+ *
+ * Layout: Q [B, Hq, Sq, D], K and V [B, Hkv, Skv, D], all contiguous
+ * row-major 16-bit patterns. Outputs are double and unrounded.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_FP16 0
+#define ORACLE_BF16 1
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_fp16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double x;
+    if (e == 0)
+        x = ldexp((double)m, -24); /* subnormal: m * 2^-14 * 2^-10 */
+    else if (e == 31)
+        x = m ? NAN : INFINITY;
+    else
+        x = ldexp((double)(m | 0x400), e - 25); /* (1024 + m) * 2^(e-15-10) */
+    return sign ? -x : x;
+}
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
+double oracle_bf16_to_double(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int m = b & 0x7f;
+    double x;
+    if (e == 0)
+        x = ldexp((double)m, -133); /* subnormal: m * 2^-126 * 2^-7 */
+    else if (e == 255)
+        x = m ? NAN : INFINITY;
+    else
+        x = ldexp((double)(m | 0x80), e - 134); /* (128 + m) * 2^(e-127-7) */
+    return sign ? -x : x;
+}
+
+static double decode(uint16_t bits, int dtype)
+{
+    return dtype == ORACLE_BF16 ? oracle_bf16_to_double(bits) : oracle_fp16_to_double(bits);
+}
+
+/*
+ * One query row against one KV head, straight from the definition above.
+ * p receives the Skv softmax weights exp(s_j - M) / L.
+ */
+static void attend_row(const double *q, const double *Kg, const double *Vg, int Skv, int D,
+                       double scale, double *s, double *p, double *o, double *lse)
+{
+    /* scores */
+    for (int j = 0; j < Skv; ++j) {
+        double acc = 0.0;
+        const double *kj = Kg + (size_t)j * D;
+        for (int d = 0; d < D; ++d)
+            acc += q[d] * kj[d];
+        s[j] = scale * acc;
+    }
+    /* row maximum */
+    double M = -INFINITY;
+    for (int j = 0; j < Skv; ++j)
+        if (s[j] > M)
+            M = s[j];
+    /* exponentials and their sum */
+    double L = 0.0;
+    for (int j = 0; j < Skv; ++j) {
+        p[j] = exp(s[j] - M);
+        L += p[j];
+    }
+    /* weighted sum of value rows, then normalise */
+    for (int d = 0; d < D; ++d)
+        o[d] = 0.0;
+    for (int j = 0; j < Skv; ++j) {
+        const double *vj = Vg + (size_t)j * D;
+        for (int d = 0; d < D; ++d)
+            o[d] += p[j] * vj[d];
+    }
+    for (int d = 0; d < D; ++d)
+        o[d] /= L;
+    for (int j = 0; j < Skv; ++j)
+        p[j] /= L;
+    *lse = M + log(L);
+}
+
+static int check_shape(int B, int Hq, int Hkv, int Sq, int Skv, int D, int dtype)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || D <= 0)
+        return -1;
+    if (Hq % Hkv != 0)
+        return -1;
+    if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16)
+        return -1;
+    return 0;
+}
+
+/*
+ * Attention forward on a chosen set of query rows.
+ *
+ * rows:   int32 [B*Hq*nrows], the query-row indices evaluated for each (b, h),
+ *         in (b, h) order; every index must lie in [0, Sq).
+ * o_out:  double [B*Hq*nrows*D], O for those rows in the same order.
+ * lse_out: double [B*Hq*nrows] (may be NULL).
+ * Returns 0, or -1 on a bad shape or row index.
+ */
+int oracle_sdp_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                        int B, int Hq, int Hkv, int Sq, int Skv, int D, double scale,
+                        const int32_t *rows, int nrows, double *o_out, double *lse_out)
+{
+    if (check_shape(B, Hq, Hkv, Sq, Skv, D, dtype) || nrows < 0)
+        return -1;
+    for (long t = 0; t < (long)B * Hq * nrows; ++t)
+        if (rows[t] < 0 || rows[t] >= Sq)
+            return -1;
+    const int G = Hq / Hkv;
+    double *Kg = (double *)malloc(sizeof(double) * (size_t)Skv * D);
+    double *Vg = (double *)malloc(sizeof(double) * (size_t)Skv * D);
+    if (!Kg || !Vg) {
+        free(Kg);
+        free(Vg);
+        return -1;
+    }
+    int status = 0;
+    for (int b = 0; b < B && !status; ++b) {
+        for (int g = 0; g < Hkv && !status; ++g) {
+            const size_t kv_off = ((size_t)b * Hkv + g) * (size_t)Skv * D;
+            const long nkv = (long)Skv * D;
+#pragma omp parallel for schedule(static)
+            for (long t = 0; t < nkv; ++t) {
+                Kg[t] = decode(k[kv_off + t], dtype);
+                Vg[t] = decode(v[kv_off + t], dtype);
+            }
+            /* every (query head of this group, sampled row) pair */
+            const long npairs = (long)G * nrows;
+#pragma omp parallel
+            {
+                double *qrow = (double *)malloc(sizeof(double) * D);
+                double *s = (double *)malloc(sizeof(double) * Skv);
+                double *p = (double *)malloc(sizeof(double) * Skv);
+                int ok = qrow && s && p;
+                if (!ok) {
+#pragma omp atomic write
+                    status = -1;
+                }
+#pragma omp for schedule(dynamic, 1)
+                for (long t = 0; t < npairs; ++t) {
+                    if (!ok)
+                        continue;
+                    const int h = g * G + (int)(t / nrows);
+                    const long slot = ((long)b * Hq + h) * nrows + (t % nrows);
+                    const int i = rows[slot];
+                    const size_t q_off = (((size_t)b * Hq + h) * (size_t)Sq + i) * D;
+                    for (int d = 0; d < D; ++d)
+                        qrow[d] = decode(q[q_off + d], dtype);
+                    double lse;
+                    attend_row(qrow, Kg, Vg, Skv, D, scale, s, p, o_out + (size_t)slot * D, &lse);
+                    if (lse_out)
+                        lse_out[slot] = lse;
+                }
+                free(qrow);
+                free(s);
+                free(p);
+            }
+        }
+    }
+    free(Kg);
+    free(Vg);
+    return status;
+}
+
+/*
+ * The softmax weights of one query row (b, h, i): p_out double [Skv].
+ * Exposed so that properties of the weights themselves can be checked.
+ */
+int oracle_sdp_row_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                         int B, int Hq, int Hkv, int Sq, int Skv, int D, double scale,
+                         int b, int h, int i, double *p_out, double *o_out, double *lse_out)
+{
+    if (check_shape(B, Hq, Hkv, Sq, Skv, D, dtype))
+        return -1;
+    if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Sq)
+        return -1;
+    const int g = h / (Hq / Hkv);
+    const size_t kv_off = ((size_t)b * Hkv + g) * (size_t)Skv * D;
+    const size_t q_off = (((size_t)b * Hq + h) * (size_t)Sq + i) * D;
+    double *Kg = (double *)malloc(sizeof(double) * (size_t)Skv * D);
+    double *Vg = (double *)malloc(sizeof(double) * (size_t)Skv * D);
+    double *qrow = (double *)malloc(sizeof(double) * D);
+    double *s = (double *)malloc(sizeof(double) * Skv);
+    int status = -1;
+    if (Kg && Vg && qrow && s) {
+        for (size_t t = 0; t < (size_t)Skv * D; ++t) {
+            Kg[t] = decode(k[kv_off + t], dtype);
+            Vg[t] = decode(v[kv_off + t], dtype);
+        }
+        for (int d = 0; d < D; ++d)
+            qrow[d] = decode(q[q_off + d], dtype);
+        attend_row(qrow, Kg, Vg, Skv, D, scale, s, p_out, o_out, lse_out);
+        status = 0;
+    }
+    free(Kg);
+    free(Vg);
+    free(qrow);
+    free(s);
+    return status;
+}
+
+/* Threads an OpenMP parallel region of the oracle uses (1 without OpenMP). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
