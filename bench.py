@@ -1,0 +1,348 @@
+"""Benchmark of the fused grouped-query attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one sdp_fwd launch over the whole workload (every query head,
+every query row, every key). The default workload is the pages' headline
+shape: 32 query heads over 2 KV heads, head dim 256, Sq = Skv = 16384, fp16,
+non-causal, scale 1/16. Prints one JSON line (rank 0).
+
+Throughput counts 4 * Sq * Skv * D FLOPs per (batch, query head). Inputs are
+synthetic and seeded (N(0,1) rounded to the I/O dtype). Q and O are 268 MB
+each, larger than the 126 MB L2, so no explicit flush runs between steps.
+
+--impl reference times the fp64 CPU oracle (the only other implementation
+that exists for this path) on the host cores, on a bounded sample of query
+rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gqa_flash_attention_gb300 import workloads  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense fp16/bf16 tensor peak"
+FALLBACK_PEAK_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--cpu-rows", type=int, default=0, help="query rows per head in the CPU sample (0: auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), "measured"
+    return FALLBACK_PEAK_TFLOPS, 1700.0, "fallback"
+
+
+def source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gqa_flash_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"sdp_fwd_{workload}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("source_hash") != source_hash():
+        return None
+    try:
+        return int(float(kv["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.uuid = None
+        try:
+            self.uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            pass
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                pw.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_rows_auto(w):
+    # about 10-20 s of oracle work on a 16-core host at ~1 fp64 GFLOP/s per core
+    per_row = 4.0 * w.Skv * w.D
+    target = 1.5e11
+    return int(max(2, min(w.Sq, target / (per_row * w.B * w.Hq))))
+
+
+def run_cpu_oracle(w, rows_per_head, q=None, k=None, v=None):
+    """Time the oracle on a sample of query rows; returns (tflops, seconds, rows, threads)."""
+    import oracle
+    if q is None:
+        q, k, v = workloads.make_inputs(w)
+    rows = workloads.sample_rows(w, rows_per_head, seed=1234)
+    dt = oracle.FP16 if w.dtype == "fp16" else oracle.BF16
+    t0 = time.perf_counter()
+    oracle.sdp_fwd_rows(q, k, v, dt, w.shape, w.softmax_scale, rows)
+    sec = time.perf_counter() - t0
+    flops = 4.0 * w.B * w.Hq * rows.shape[2] * w.Skv * w.D
+    return flops / sec / 1e12, sec, rows.shape[2], oracle.num_threads()
+
+
+# ------------------------------------------------------------------ arms
+
+def reference_arm(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    rows = args.cpu_rows or max(2, cpu_rows_auto(w) // 4)
+    q, k, v = workloads.make_inputs(w)
+    for _ in range(args.warmup):
+        run_cpu_oracle(w, max(2, rows // 8), q, k, v)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        tf, sec, nrows, threads = run_cpu_oracle(w, rows, q, k, v)
+        vals.append(tf)
+        secs.append(sec)
+    value = statistics.median(vals)
+    sample = (f"{nrows} query rows per (batch, head) x {w.B * w.Hq} heads of {w.name}, all {w.Skv} keys, "
+              f"per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.median(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, n):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv, "D": w.D,
+            "io_dtype": w.dtype, "scale": w.softmax_scale, "causal": False, "peaky_k": w.peaky_k,
+            "flops_per_step_per_gpu": w.flops(), "l2": "inputs larger than L2 (Q and O exceed 126 MB); no flush",
+            "parallelism": "replicas" if n > 1 else "single GPU"}
+
+
+def ours_arm(args, w):
+    import gqa_flash_attention_gb300 as sdp
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    sdp.lib()
+
+    q_h, k_h, v_h = workloads.make_inputs(w)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse)
+    torch.cuda.synchronize(dev)
+    if sdp.poll_status() != sdp.SDP_OK:
+        raise RuntimeError("kernel reported a timeout during warm-up")
+
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for i in range(K):
+        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
+    total_ms = ev[0].elapsed_time(ev[K])
+    if sdp.poll_status() != sdp.SDP_OK:
+        raise RuntimeError("kernel reported a timeout in the timed region")
+
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    max_total_ms = float(t.item())
+    ms_per_step = max_total_ms / K
+    value = world * w.flops() / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, O and LSE back to pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+        op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        n_e2e = max(3, K // 10)
+
+        def e2e_step():
+            q.copy_(qp, non_blocking=True)
+            k.copy_(kp, non_blocking=True)
+            v.copy_(vp, non_blocking=True)
+            sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse)
+            op.copy_(o, non_blocking=True)
+            lp.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        te = torch.tensor([e0.elapsed_time(e1) / n_e2e], dtype=torch.float64, device=dev)
+        if world > 1:
+            torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+        h2d = sum(t_.numel() * t_.element_size() for t_ in (q_h, k_h, v_h))
+        d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+        e2e = {"value": world * w.flops() / (float(te.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peak, peak_sus, peak_src = load_peaks()
+    avg_launch_ms = statistics.mean(per_launch_ms)
+    achieved = w.flops() / (avg_launch_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": load_traffic(w.name),
+                "peak_source": f"{peak_src} bf16 dense (burst); fp16 runs at the same tensor rate",
+                "frac_of_sustained": achieved / peak_sus, "kernel": "sdp_fwd_kernel",
+                "launch_ms_median": statistics.median(per_launch_ms)}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rows = args.cpu_rows or cpu_rows_auto(w)
+        tf, sec, nrows, threads = run_cpu_oracle(w, rows, q_h, k_h, v_h)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{nrows} query rows per (batch, head) x {w.B * w.Hq} heads of {w.name}, all {w.Skv} "
+                         f"keys ({sec:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic", "config": config_of(w, world),
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": K,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w)
+    else:
+        ours_arm(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,162 @@
-"""placeholder"""
+"""GB300-native fused grouped-query attention forward.
+
+``sdp_fwd(q, k, v)`` computes O = softmax(Q K^T * scale) V and the natural
+log-sum-exp of every score row for query heads that share KV heads in
+groups of Hq / Hkv. The work runs in ``libsdp.so`` (hand-written CUDA for
+sm_103a: TMA, mbarriers, tcgen05 MMAs with TMEM accumulators); this module
+only checks and marshals arguments through the C ABI of ``include/sdp.h``.
+PyTorch supplies device memory and streams. There is no fallback: if the
+library is missing or the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = ["sdp_fwd", "sdp_fwd_ptr", "poll_status", "SdpError", "lib", "LIB_PATH", "SDP_FP16", "SDP_BF16",
+           "set_wait_timeout_ms", "set_debug_flags", "last_status_detail", "strerror"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsdp.so")
+
+SDP_FP16 = 0
+SDP_BF16 = 1
+SDP_OK = 0
+SDP_ERR_INVALID_ARG = -1
+SDP_ERR_UNSUPPORTED = -2
+SDP_ERR_ALIGNMENT = -3
+SDP_ERR_OVERFLOW = -4
+SDP_ERR_CUDA = -5
+SDP_ERR_DEVICE_TIMEOUT = -6
+
+_DTYPE_CODE = {torch.float16: SDP_FP16, torch.bfloat16: SDP_BF16}
+
+_lib = None
+
+
+class SdpError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"sdp error {code}: {msg}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libsdp.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run `python -m gqa_flash_attention_gb300.build` "
+                               "(the CUDA library is required; there is no fallback path)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.sdp_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        L.sdp_fwd.restype = i
+        L.sdp_poll_status.argtypes = [vp]
+        L.sdp_poll_status.restype = i
+        L.sdp_last_status_detail.argtypes = []
+        L.sdp_last_status_detail.restype = ctypes.c_uint
+        L.sdp_set_wait_timeout_ms.argtypes = [ctypes.c_uint]
+        L.sdp_set_wait_timeout_ms.restype = ctypes.c_uint
+        L.sdp_set_debug_flags.argtypes = [i]
+        L.sdp_set_debug_flags.restype = i
+        L.sdp_last_cuda_error.argtypes = []
+        L.sdp_last_cuda_error.restype = i
+        L.sdp_strerror.argtypes = [i]
+        L.sdp_strerror.restype = ctypes.c_char_p
+        L.sdp_version.argtypes = []
+        L.sdp_version.restype = i
+        L.sdp_shutdown.argtypes = []
+        L.sdp_shutdown.restype = None
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().sdp_strerror(int(code)).decode()
+
+
+def _check(rc: int) -> None:
+    if rc != SDP_OK:
+        msg = strerror(rc)
+        if rc == SDP_ERR_CUDA:
+            msg += f" (cudaError {lib().sdp_last_cuda_error()})"
+        raise SdpError(rc, msg)
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def sdp_fwd_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
+                scale: float, dtype: int, stream: int = 0) -> int:
+    """The raw C call with integer addresses; returns the status code."""
+    return int(lib().sdp_fwd(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.c_void_p(o),
+                             ctypes.c_void_p(lse), int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(D),
+                             ctypes.c_float(scale), int(dtype), ctypes.c_void_p(stream)))
+
+
+def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+            out: torch.Tensor | None = None, lse: torch.Tensor | None = None, return_lse: bool = True,
+            stream=None):
+    """Grouped-query attention forward on sm_103a.
+
+    q: [B, Hq, Sq, D]; k, v: [B, Hkv, Skv, D]; fp16 or bf16, contiguous, on one
+    CUDA device; D in {128, 256}; Hq a multiple of Hkv. Returns (o, lse) with o
+    like q and lse fp32 [B, Hq, Sq] (None when return_lse is False and no lse
+    buffer is given). The work is enqueued on `stream` (default: the current
+    stream) and not synchronised.
+    """
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, S, D]")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda) or not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be CUDA tensors on one device")
+    if q.dtype not in _DTYPE_CODE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, float16 or bfloat16")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, Hq, Sq, D = q.shape
+    if k.shape[0] != B or k.shape[3] != D or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    Hkv, Skv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != q.device:
+        raise ValueError("out must be a contiguous tensor shaped and typed like q")
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.shape != (B, Hq, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous()
+                            or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 tensor [B, Hq, Sq] on q's device")
+    with torch.cuda.device(q.device):
+        rc = sdp_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         0 if lse is None else lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
+                         _DTYPE_CODE[q.dtype], _stream_handle(stream, q.device))
+    _check(rc)
+    return out, lse
+
+
+def poll_status(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().sdp_poll_status(ctypes.c_void_p(_stream_handle(stream, dev))))
+
+
+def last_status_detail() -> int:
+    return int(lib().sdp_last_status_detail())
+
+
+def set_wait_timeout_ms(ms: int) -> int:
+    return int(lib().sdp_set_wait_timeout_ms(int(ms)))
+
+
+def set_debug_flags(flags: int) -> int:
+    return int(lib().sdp_set_debug_flags(int(flags)))

@@ -1,0 +1,521 @@
+// Fused grouped-query attention forward for sm_103a (GB300).
+//
+// One CTA computes one unit = (batch b, query head h, 128 query rows). It
+// streams the 128-key tiles of KV head g = h / (Hq/Hkv) once, keeping the
+// online-softmax state (row maximum m, row sum l) in fp32 registers and the
+// output accumulator O in tensor memory ("xe2-sdp-hd256" page, section
+// "HD=256 Architecture Differences": single pass over KV chunks of 128 with a
+// 128-row Q tile held on chip; "xe2-sdp-bf16" page, section "Data flow
+// diagram": 16-bit operands into the contractions, fp32 softmax, output
+// rounded to the input type at the very end).
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax, lazy O rescale, epilogue. Thread t owns query row t,
+//              which is TMEM lane t (warp w may only touch lanes 32w..32w+31).
+//   warp 4     TMA producer: Q once, then K/V chunks through a ring of
+//              32 KB shared-memory slots (full/empty mbarriers).
+//   warp 5     tcgen05 MMA issuer (one thread) and TMEM owner.
+//
+// Per KV tile j the tensor core runs S_j = Q K_j^T (SMEM x SMEM -> TMEM fp32)
+// and O += P_j V_j (P from TMEM, V from SMEM). S is double-buffered in TMEM so
+// that S_{j+1} is computed while the softmax of tile j runs; P_j overwrites
+// the first 64 columns of S_j's buffer as packed 16-bit pairs.
+//
+// Every mbarrier wait is bounded: after the timeout the waiting thread
+// records a status code, raises a CTA-wide abort flag, and every role leaves
+// its loop, drains what it has in flight, frees TMEM and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "sdp_launch.h"
+
+namespace sdp {
+
+
+enum : uint32_t {
+    SITE_Q_FULL = 1,
+    SITE_SLOT_EMPTY = 2,
+    SITE_SLOT_FULL = 3,
+    SITE_S_FULL = 4,
+    SITE_P_FULL = 5,
+    SITE_O_DONE = 6,
+};
+
+constexpr int DEBUG_NO_LOADS = 1;
+
+template <int D>
+struct Layout {
+    static constexpr int BM = 128;                        // query rows per unit
+    static constexpr int BN = 128;                        // keys per KV tile
+    static constexpr int BOX_COLS = 64;                   // one 128-byte swizzle row of 16-bit values
+    static constexpr int BOX_BYTES = 128 * BOX_COLS * 2;  // 16 KB: 128 rows x 64 columns
+    static constexpr int CHUNK_BYTES = 2 * BOX_BYTES;     // 32 KB: 128 rows x 128 columns
+    static constexpr int CHUNKS_PER_TILE = D / 128;       // ring chunks per K (or V) tile
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int SMEM_LIMIT = 227 * 1024;
+    static constexpr int NSLOTS = (SMEM_LIMIT - 2048 - Q_BYTES) / CHUNK_BYTES;
+    static constexpr int BAR_OFF = Q_BYTES + NSLOTS * CHUNK_BYTES;
+    static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // barriers, then slack to align the base to 1 KB
+    static constexpr int TM_O = 0;                           // O accumulator: columns [0, D)
+    static constexpr int TM_S = D;                           // S/P buffer b: columns [D + 128b, D + 128b + 128)
+    static constexpr int TMEM_COLS = 512;
+    static_assert(D == 128 || D == 256, "head dim");
+    static_assert(NSLOTS >= 2, "ring");
+    static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
+    static_assert(D + 2 * BN <= TMEM_COLS, "tensor memory");
+    static_assert(8 * (2 * NSLOTS + 7) + 8 <= 256, "barrier area");
+};
+
+// Lazy rescale threshold in base-2 units: the running maximum is only moved
+// when a tile's maximum exceeds it by more than this, so P <= 2^8.
+constexpr float RESCALE_THRESHOLD = 8.0f;
+constexpr float LN2 = 0.6931471805599453f;
+
+struct WaitCtx {
+    volatile int *abort_flag;
+    unsigned int *status;
+    unsigned long long timeout_ns;
+};
+
+// Slow path of wait_bounded: poll until the phase completes, the CTA aborts,
+// or the timeout passes (then raise the abort flag and record `site` and the
+// CTA index in the status word).
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned int *status,
+                                       unsigned long long timeout_ns, uint32_t site)
+{
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1;
+                const uint32_t cta = blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu;
+                atomicCAS(status, 0u, site | (cta << 8));
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait for the phase of `bar` with parity `parity`; false if the CTA
+// is aborting or the wait ran out.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx &cx, uint32_t site)
+{
+    if (ptx::mbar_try_wait(bar, parity))
+        return true;
+    return wait_slow(bar, parity, cx.abort_flag, cx.status, cx.timeout_ns, site);
+}
+
+// Bounded wait that ignores the abort flag: used only to drain copies and MMAs
+// this thread issued itself, which always complete.
+static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns)
+{
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > timeout_ns)
+            return false;
+    }
+    return true;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    if constexpr (BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
+        return *reinterpret_cast<uint32_t *>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(192, 1)
+    sdp_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const KernelParams p)
+{
+    using L = Layout<D>;
+    constexpr int NS = L::NSLOTS;
+    constexpr int CPT = L::CHUNKS_PER_TILE;
+    constexpr uint32_t IDESC_S = ptx::idesc_f16_f32acc(128, L::BN, BF16, false);  // Q (K-major) x K (K-major)
+    constexpr uint32_t IDESC_PV = ptx::idesc_f16_f32acc(128, 128, BF16, true);    // P (TMEM) x V (N-major)
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw_addr + pad;
+    const uint32_t s_q = sbase;  // Q tile; reused as the O staging tile in the epilogue
+    const uint32_t s_ring = sbase + L::Q_BYTES;
+    const uint32_t bar0 = sbase + L::BAR_OFF;
+    const uint32_t q_full = bar0;
+    const uint32_t slot_full0 = bar0 + 8u;
+    const uint32_t slot_empty0 = bar0 + 8u * (1 + NS);
+    const uint32_t s_full0 = bar0 + 8u * (1 + 2 * NS);
+    const uint32_t p_full0 = bar0 + 8u * (3 + 2 * NS);
+    const uint32_t o_done = bar0 + 8u * (5 + 2 * NS);
+    const uint32_t final_bar = bar0 + 8u * (6 + 2 * NS);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * (7 + 2 * NS));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Unit order: head-in-group fastest, then query tile, then (batch, KV head),
+    // so CTAs resident together read the same K/V tiles from L2.
+    int u = blockIdx.x;
+    const int hi = u % p.G;
+    u /= p.G;
+    const int qt = u % p.n_qtiles;
+    const int bg = u / p.n_qtiles;  // b * Hkv + g
+    const int b = bg / p.Hkv;
+    const int g = bg - b * p.Hkv;
+    const int z_q = b * p.Hq + g * p.G + hi;  // (b, h) plane of Q, O and LSE
+    const int z_kv = bg;                      // (b, g) plane of K and V
+    const int q0 = qt * L::BM;
+    const int n = p.n_kvtiles;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(q_full, 1);
+        for (int s = 0; s < NS; ++s) {
+            ptx::mbar_init(slot_full0 + 8u * s, 1);
+            ptx::mbar_init(slot_empty0 + 8u * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(s_full0 + 8u * i, 1);
+            ptx::mbar_init(p_full0 + 8u * i, 128);
+        }
+        ptx::mbar_init(o_done, 1);
+        ptx::mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 4 && lane == 0) {
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+        ptx::prefetch_tmap(&tm_o);
+    }
+    if (warp == 5) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), L::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const WaitCtx cx{abort_flag, p.status, p.timeout_ns};
+
+    if (warp == 4) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int slot = 0;
+            uint32_t ph = 0, armed_mask = 0, armed_par = 0;
+            bool q_armed = false;
+            if (!(p.debug_flags & DEBUG_NO_LOADS)) {
+                ptx::mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+#pragma unroll
+                for (int c = 0; c < D / L::BOX_COLS; ++c)
+                    ptx::tma_load_3d(s_q + c * L::BOX_BYTES, &tm_q, q_full, c * L::BOX_COLS, q0, z_q);
+                q_armed = true;
+                // Load order = MMA consumption order: K_0, then per j: K_{j+1}, V_j.
+                auto load_tile = [&](const CUtensorMap *map, int j) -> bool {
+#pragma unroll
+                    for (int ch = 0; ch < CPT; ++ch) {
+                        const uint32_t full = slot_full0 + 8u * slot;
+                        if (!wait_bounded(slot_empty0 + 8u * slot, ph ^ 1u, cx, SITE_SLOT_EMPTY))
+                            return false;
+                        ptx::mbar_arrive_expect_tx(full, L::CHUNK_BYTES);
+                        const uint32_t dst = s_ring + slot * L::CHUNK_BYTES;
+                        ptx::tma_load_3d(dst, map, full, ch * 128, j * L::BN, z_kv);
+                        ptx::tma_load_3d(dst + L::BOX_BYTES, map, full, ch * 128 + L::BOX_COLS, j * L::BN, z_kv);
+                        armed_mask |= 1u << slot;
+                        armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
+                        if (++slot == NS) {
+                            slot = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    return true;
+                };
+                bool ok = load_tile(&tm_k, 0);
+                for (int j = 0; ok && j < n; ++j) {
+                    if (j + 1 < n)
+                        ok = load_tile(&tm_k, j + 1);
+                    if (ok)
+                        ok = load_tile(&tm_v, j);
+                }
+            }
+            // Every copy this thread issued lands before the CTA may exit.
+            if (q_armed)
+                wait_drain(q_full, 0, p.timeout_ns);
+            for (int s = 0; s < NS; ++s)
+                if (armed_mask & (1u << s))
+                    wait_drain(slot_full0 + 8u * s, (armed_par >> s) & 1u, p.timeout_ns);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int slot = 0;
+            uint32_t ph = 0;
+            bool issued = false;
+            auto advance = [&]() {
+                if (++slot == NS) {
+                    slot = 0;
+                    ph ^= 1u;
+                }
+            };
+            // S_j = Q K_j^T into S buffer j&1; K-steps of 16 along D.
+            auto issue_s = [&](int j) -> bool {
+                const uint32_t d_tmem = tmem + L::TM_S + (j & 1) * L::BN;
+#pragma unroll
+                for (int ch = 0; ch < CPT; ++ch) {
+                    if (!wait_bounded(slot_full0 + 8u * slot, ph, cx, SITE_SLOT_FULL))
+                        return false;
+                    ptx::tc_fence_after();
+                    const uint32_t kbase = s_ring + slot * L::CHUNK_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t box = kk >> 2, off = (kk & 3) * 32;
+                        const uint64_t ad = ptx::smem_desc_sw128(s_q + (2 * ch + box) * L::BOX_BYTES + off, 16, 1024);
+                        const uint64_t bd = ptx::smem_desc_sw128(kbase + box * L::BOX_BYTES + off, 16, 1024);
+                        ptx::mma_ss(d_tmem, ad, bd, IDESC_S, (ch | kk) != 0);
+                    }
+                    issued = true;
+                    ptx::mma_commit(slot_empty0 + 8u * slot);
+                    advance();
+                }
+                ptx::mma_commit(s_full0 + 8u * (j & 1));
+                return true;
+            };
+            // O[:, 128ch : 128ch+128] += P_j V_j[:, 128ch : 128ch+128]; K-steps of 16 keys.
+            auto issue_pv = [&](int j) -> bool {
+                const uint32_t a_tmem = tmem + L::TM_S + (j & 1) * L::BN;
+#pragma unroll
+                for (int ch = 0; ch < CPT; ++ch) {
+                    if (!wait_bounded(slot_full0 + 8u * slot, ph, cx, SITE_SLOT_FULL))
+                        return false;
+                    ptx::tc_fence_after();
+                    const uint32_t vbase = s_ring + slot * L::CHUNK_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bd = ptx::smem_desc_sw128(vbase + kk * 2048, L::BOX_BYTES, 1024);
+                        ptx::mma_ts(tmem + L::TM_O + ch * 128, a_tmem + kk * 8, bd, IDESC_PV, (j > 0) || (kk > 0));
+                    }
+                    issued = true;
+                    ptx::mma_commit(slot_empty0 + 8u * slot);
+                    advance();
+                }
+                ptx::mma_commit(o_done);
+                return true;
+            };
+
+            bool ok = wait_bounded(q_full, 0, cx, SITE_Q_FULL);
+            if (ok)
+                ok = issue_s(0);
+            for (int j = 0; ok && j < n; ++j) {
+                if (j + 1 < n && !(ok = issue_s(j + 1)))
+                    break;
+                if (!(ok = wait_bounded(p_full0 + 8u * (j & 1), (j >> 1) & 1, cx, SITE_P_FULL)))
+                    break;
+                ptx::tc_fence_after();
+                ok = issue_pv(j);
+            }
+            if (issued) {  // all MMAs complete before TMEM is freed
+                ptx::mma_commit(final_bar);
+                wait_drain(final_bar, 0, p.timeout_ns);
+            }
+        }
+    } else {
+        // --------------------------------------- softmax / correction / epilogue
+        const int row = threadIdx.x;  // query row within the tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + L::TM_S;
+        const uint32_t t_o = tmem + lane_off + L::TM_O;
+        const float c = p.c;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+
+        for (int j = 0; j < n; ++j) {
+            ok = wait_bounded(s_full0 + 8u * (j & 1), (j >> 1) & 1, cx, SITE_S_FULL);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok)
+                break;
+            ptx::tc_fence_after();
+            const uint32_t ts = t_s + (j & 1) * L::BN;
+            uint32_t sr[128];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                ptx::tmem_ld32(ts + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * q]));
+            ptx::tmem_wait_ld();
+            float s[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+                s[i] = __uint_as_float(sr[i]);
+
+            const int valid = p.Skv - j * L::BN;  // >= 1
+            if (valid < L::BN) {
+#pragma unroll
+                for (int i = 1; i < 128; ++i)
+                    if (i >= valid)
+                        s[i] = s[0];  // neutral for the max; weights zeroed below
+            }
+            float mx0, mx1, mx2, mx3;
+            if (c >= 0.f) {
+                mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int i = 4; i < 128; i += 4) {
+                    mx0 = fmaxf(mx0, s[i]);
+                    mx1 = fmaxf(mx1, s[i + 1]);
+                    mx2 = fmaxf(mx2, s[i + 2]);
+                    mx3 = fmaxf(mx3, s[i + 3]);
+                }
+                mx0 = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            } else {
+                mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int i = 4; i < 128; i += 4) {
+                    mx0 = fminf(mx0, s[i]);
+                    mx1 = fminf(mx1, s[i + 1]);
+                    mx2 = fminf(mx2, s[i + 2]);
+                    mx3 = fminf(mx3, s[i + 3]);
+                }
+                mx0 = fminf(fminf(mx0, mx1), fminf(mx2, mx3));
+            }
+            const float m_tile = mx0 * c;  // this tile's row maximum of s * scale * log2(e)
+            const float m_new = (j == 0 || m_tile > m_used + RESCALE_THRESHOLD) ? m_tile : m_used;
+            const float alpha = (j == 0 || m_new == m_used) ? 1.f : ptx::ex2(m_used - m_new);
+            const float neg_m = -m_new;
+
+            uint32_t pk[64];
+            float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 64; i += 2) {
+                float p0 = ptx::ex2(fmaf(s[2 * i], c, neg_m));
+                float p1 = ptx::ex2(fmaf(s[2 * i + 1], c, neg_m));
+                float p2 = ptx::ex2(fmaf(s[2 * i + 2], c, neg_m));
+                float p3 = ptx::ex2(fmaf(s[2 * i + 3], c, neg_m));
+                if (valid < L::BN) {
+                    p0 = (2 * i < valid) ? p0 : 0.f;
+                    p1 = (2 * i + 1 < valid) ? p1 : 0.f;
+                    p2 = (2 * i + 2 < valid) ? p2 : 0.f;
+                    p3 = (2 * i + 3 < valid) ? p3 : 0.f;
+                }
+                sum0 += p0;
+                sum1 += p1;
+                sum2 += p2;
+                sum3 += p3;
+                pk[i] = pack2<BF16>(p0, p1);
+                pk[i + 1] = pack2<BF16>(p2, p3);
+            }
+            ptx::tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            ptx::tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            ptx::tmem_wait_st();
+            const float tile_sum = (sum0 + sum1) + (sum2 + sum3);
+            l = (j == 0) ? tile_sum : fmaf(l, alpha, tile_sum);
+
+            if (j > 0) {
+                // O must hold PV_{j-1} before it is rescaled and PV_j accumulates on it.
+                ok = wait_bounded(o_done, (j - 1) & 1, cx, SITE_O_DONE);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok)
+                    break;
+                ptx::tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(t_o + 32 * cc, o);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        ptx::tmem_st32(t_o + 32 * cc, o);
+                    }
+                    ptx::tmem_wait_st();
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(p_full0 + 8u * (j & 1));
+            m_used = m_new;
+        }
+
+        // ------------------------------------------------------------ epilogue
+        ptx::named_bar_sync(1, 128);
+        ok = ok && !*abort_flag;
+        if (ok) {
+            ok = wait_bounded(o_done, (n - 1) & 1, cx, SITE_O_DONE);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            ptx::tc_fence_after();
+            const float inv_l = 1.f / l;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                ptx::tmem_ld32(t_o + 32 * cc, o);
+                ptx::tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                // 32 columns = four 16-byte units of row `row` in box cc/2, 128-byte swizzled.
+                const uint32_t row_addr = s_q + (cc >> 1) * L::BOX_BYTES + row * 128;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const uint32_t unit = static_cast<uint32_t>((cc & 1) * 4 + v);
+                    st_shared_v4(row_addr + ((unit ^ static_cast<uint32_t>(row & 7)) << 4), pk[4 * v], pk[4 * v + 1],
+                                 pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+            if (p.lse != nullptr && q0 + row < p.Sq)
+                p.lse[static_cast<size_t>(z_q) * p.Sq + q0 + row] = (m_used + ptx::lg2(l)) * LN2;
+            ptx::fence_proxy_async_smem();
+        }
+        ptx::named_bar_sync(1, 128);
+        if (threadIdx.x == 0 && !*abort_flag) {
+#pragma unroll
+            for (int c2 = 0; c2 < D / L::BOX_COLS; ++c2)
+                ptx::tma_store_3d(&tm_o, s_q + c2 * L::BOX_BYTES, c2 * L::BOX_COLS, q0, z_q);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_all();
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+// Host-side launcher, one instantiation per (head dim, dtype).
+template <int D, bool BF16>
+cudaError_t launch_sdp_fwd(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o,
+                           const KernelParams &p, int grid, cudaStream_t stream)
+{
+    auto kern = sdp_fwd_kernel<D, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<grid, 192, Layout<D>::SMEM_BYTES, stream>>>(q, k, v, o, p);
+    return cudaGetLastError();
+}
+
+}  // namespace sdp

@@ -1,0 +1,32 @@
+// Internal interface between the C ABI (sdp_api.cu) and the per-instantiation
+// kernel translation units. Not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sdp {
+
+// Arguments of one launch beyond the four tensor maps.
+struct KernelParams {
+    float *lse;            // [B, Hq, Sq] fp32, or nullptr
+    unsigned int *status;  // device status word (0 = fine)
+    int Hq, Hkv, G, Sq, Skv;
+    int n_qtiles, n_kvtiles;
+    float c;  // scale * log2(e): scores in base-2 units
+    unsigned long long timeout_ns;
+    int debug_flags;
+};
+
+#define SDP_DECLARE_LAUNCH(NAME)                                                                                  \
+    cudaError_t NAME(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o,       \
+                     const KernelParams &p, int grid, cudaStream_t stream);
+
+SDP_DECLARE_LAUNCH(launch_d128_fp16)
+SDP_DECLARE_LAUNCH(launch_d128_bf16)
+SDP_DECLARE_LAUNCH(launch_d256_fp16)
+SDP_DECLARE_LAUNCH(launch_d256_bf16)
+
+#undef SDP_DECLARE_LAUNCH
+
+}  // namespace sdp

@@ -1,0 +1,116 @@
+/*
+ * sdp.h — C ABI of libsdp.so: fused grouped-query scaled-dot-product
+ * attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("xe2-sdp-hd256" page, header and sections "HD=256
+ * Architecture Differences" and "Performance Testing"; "xe2-sdp-bf16" page,
+ * sections "Kernel Architecture: bf16io" and "Data flow diagram"): for batch
+ * b, query head h, query row i, with G = Hq / Hkv and g = h / G,
+ *
+ *     s_j      = scale * <Q[b,h,i,:], K[b,g,j,:]>          0 <= j < Skv
+ *     O[b,h,i] = sum_j softmax(s)_j * V[b,g,j,:]
+ *     LSE      = ln sum_j exp(s_j)                         (natural log)
+ *
+ * The softmax statistics (row maximum, row sum) are kept in fp32; the two
+ * contractions take fp16 or bf16 operands and accumulate in fp32. O has the
+ * input dtype ("bf16io": bf16 in, bf16 out); LSE is fp32.
+ *
+ * Every pointer argument is plain memory; no framework type crosses this
+ * boundary. The calls are not re-entrant on one stream in any special way:
+ * each call only enqueues work on `stream`.
+ */
+#ifndef GQA_SDP_H
+#define GQA_SDP_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes */
+#define SDP_FP16 0
+#define SDP_BF16 1
+
+/* status codes (0 or negative) */
+#define SDP_OK 0
+#define SDP_ERR_INVALID_ARG (-1)    /* null pointer, non-positive size, Hq % Hkv != 0, non-finite scale, o aliasing q/k/v */
+#define SDP_ERR_UNSUPPORTED (-2)    /* D not 128 or 256, unknown dtype, device not sm_103 */
+#define SDP_ERR_ALIGNMENT (-3)      /* q, k, v, o not 16-byte aligned, or lse not 4-byte aligned */
+#define SDP_ERR_OVERFLOW (-4)       /* index space does not fit the kernel's 32-bit tile and coordinate counters */
+#define SDP_ERR_CUDA (-5)           /* a CUDA runtime/driver call failed; sdp_last_cuda_error() gives the code */
+#define SDP_ERR_DEVICE_TIMEOUT (-6) /* a kernel gave up on a bounded wait and flagged its status word */
+
+/*
+ * sdp_fwd — O = softmax(Q K^T * scale) V and LSE, enqueued on `stream`.
+ *
+ * q    device, [B, Hq, Sq, D], contiguous row-major, dtype elements
+ * k, v device, [B, Hkv, Skv, D], contiguous row-major, dtype elements
+ * o    device, [B, Hq, Sq, D], contiguous row-major, dtype elements (written)
+ * lse  device, [B, Hq, Sq] fp32 (written), or NULL to skip it
+ * B, Hq, Hkv, Sq, Skv >= 1 with Hq % Hkv == 0; D in {128, 256}
+ * scale  finite fp32 multiplier of the scores (1/sqrt(D) is the usual value)
+ * dtype  SDP_FP16 or SDP_BF16 (the type of q, k, v and o)
+ * stream a cudaStream_t (NULL = the legacy default stream)
+ *
+ * Ownership: all buffers belong to the caller and must stay valid until the
+ * enqueued work has finished. q, k, v are only read; o and lse are only
+ * written (never read first). o must not alias q, k or v (rejected when the
+ * pointers are equal; other overlaps are undefined).
+ *
+ * Errors: on any validation error nothing is launched and the code is
+ * returned. SDP_ERR_CUDA reports a failed tensor-map encode or launch. The
+ * call does not synchronise, so a device-side timeout is reported later by
+ * sdp_poll_status(). On the first call on a device the library allocates a
+ * 4-byte status word there (freed by sdp_shutdown()).
+ */
+int sdp_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+            int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale, int dtype,
+            void *stream);
+
+/*
+ * sdp_poll_status — synchronise `stream`, then read and clear the current
+ * device's status word. Returns SDP_OK, SDP_ERR_DEVICE_TIMEOUT (a kernel
+ * abandoned a wait after the timeout and returned without writing its
+ * tile), or SDP_ERR_CUDA (the synchronisation itself failed).
+ */
+int sdp_poll_status(void *stream);
+
+/*
+ * sdp_last_status_detail — the raw status word read by the last
+ * sdp_poll_status() that found an error: bits 0-7 name the wait that timed
+ * out (1 Q load, 2 KV slot empty, 3 KV slot full, 4 S ready, 5 P ready,
+ * 6 O done), bits 8-31 the CTA index (saturating).
+ */
+unsigned int sdp_last_status_detail(void);
+
+/*
+ * sdp_set_wait_timeout_ms — upper bound, in milliseconds, on any single wait
+ * inside the kernel (default 2000). Applies to launches made after the call.
+ * Returns the previous value. 0 restores the default.
+ */
+unsigned int sdp_set_wait_timeout_ms(unsigned int ms);
+
+/*
+ * sdp_set_debug_flags — test hooks, 0 by default. Bit 0: the load warp issues
+ * no copies at all, so every consumer wait runs out and the kernel returns
+ * through its timeout path (used to test that path without a fault).
+ * Returns the previous flags.
+ */
+int sdp_set_debug_flags(int flags);
+
+/* The CUDA error code (cudaError_t) of the last SDP_ERR_CUDA in this process. */
+int sdp_last_cuda_error(void);
+
+/* A static, human-readable description of a status code. */
+const char *sdp_strerror(int code);
+
+/* ABI version: 100 * major + minor. */
+int sdp_version(void);
+
+/* Free the per-device status words. Call only with no sdp work in flight. */
+void sdp_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_SDP_H */

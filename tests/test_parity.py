@@ -1,0 +1,132 @@
+"""CUDA path vs the fp64 oracle, through the C ABI, on the same seeded inputs.
+
+Small cases are checked element by element on every output row; they span
+several 128-row query tiles and 128-key KV tiles, ragged tails on both, and
+the degenerate one-row / one-key cases. The five full-size workloads are run
+in the same launch configuration the benchmark times and checked on a seeded
+sample of 256 query rows per (batch, head), rows 0 and Sq-1 included.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_flash_attention_gb300 as sdp
+import oracle
+from gqa_flash_attention_gb300 import workloads
+from gqa_flash_attention_gb300.workloads import Workload
+from parity import ORACLE_DTYPE, assert_within, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gqa_flash_attention_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    sdp.lib()
+
+
+def gpu_run(q, k, v, scale, guard=4096):
+    """Run through the C ABI into canary-filled buffers with guard tails."""
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    B, Hq, Sq, D = q.shape
+    o_buf = torch.full((q.numel() + guard,), float("nan"), dtype=q.dtype, device=dev)
+    l_buf = torch.full((B * Hq * Sq + guard,), float("nan"), dtype=torch.float32, device=dev)
+    o = o_buf[:q.numel()].view(q.shape)
+    lse = l_buf[:B * Hq * Sq].view(B, Hq, Sq)
+    sdp.sdp_fwd(qd, kd, vd, scale=scale, out=o, lse=lse)
+    assert sdp.poll_status() == sdp.SDP_OK
+    assert torch.isnan(o_buf[q.numel():]).all(), "write past the end of O"
+    assert torch.isnan(l_buf[B * Hq * Sq:]).all(), "write past the end of LSE"
+    return o, lse
+
+
+def check_full(w: Workload):
+    q, k, v = workloads.make_inputs(w)
+    o, lse = gpu_run(q, k, v, w.softmax_scale)
+    ref_o, ref_l = oracle.sdp_fwd(q, k, v, ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale)
+    st = compare(o, lse, ref_o, ref_l, w.dtype)
+    assert_within(st, w.dtype)
+    return st
+
+
+SMALL = []
+for D in (128, 256):
+    for dt in ("fp16", "bf16"):
+        SMALL += [
+            Workload(f"one_{D}_{dt}", 1, 2, 1, 1, 1, D, dt, seed=31),
+            Workload(f"tails_{D}_{dt}", 1, 2, 2, 127, 129, D, dt, seed=32),
+            Workload(f"gqa2_{D}_{dt}", 1, 4, 2, 129, 300, D, dt, seed=33),
+            Workload(f"gqa4_b2_{D}_{dt}", 2, 4, 1, 300, 1000, D, dt, seed=34),
+            Workload(f"gqa16_{D}_{dt}", 1, 16, 1, 64, 127, D, dt, seed=35),
+            Workload(f"mha_{D}_{dt}", 1, 4, 4, 200, 128, D, dt, seed=36),
+            Workload(f"kv1_{D}_{dt}", 1, 2, 1, 130, 1, D, dt, seed=37),
+        ]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_small_cases_every_row(w):
+    check_full(w)
+
+
+def test_smallest_workload_every_row():
+    check_full(workloads.WORKLOADS["gqa4_s256_d128_fp16"])
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.0625, 0.5])
+def test_scale_sign_and_zero(scale):
+    check_full(Workload("scale", 1, 4, 2, 150, 260, 128, "fp16", seed=41, scale=scale))
+
+
+def test_peaky_keys_small():
+    check_full(Workload("peaky", 1, 8, 2, 256, 1024, 128, "bf16", seed=42, peaky_k=True))
+
+
+@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if n != "gqa4_s256_d128_fp16"])
+def test_full_size_workload_sampled_rows(name):
+    w = workloads.WORKLOADS[name]
+    q, k, v = workloads.make_inputs(w)
+    o, lse = gpu_run(q, k, v, w.softmax_scale)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    rows = workloads.sample_rows(w, 256)
+    ref_o, ref_l = oracle.sdp_fwd_rows(q, k, v, ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale, rows)
+    idx = torch.from_numpy(rows.astype(np.int64)).to(o.device)
+    o_s = torch.gather(o, 2, idx[..., None].expand(-1, -1, -1, w.D))
+    l_s = torch.gather(lse, 2, idx)
+    st = compare(o_s, l_s, ref_o, ref_l, w.dtype)
+    assert_within(st, w.dtype)
+
+
+def test_deterministic_and_stream_aware():
+    w = Workload("det", 1, 8, 2, 300, 700, 256, "bf16", seed=43)
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    o1, l1 = sdp.sdp_fwd(q, k, v)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o2, l2 = sdp.sdp_fwd(q, k, v)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_without_lse():
+    w = Workload("nolse", 1, 4, 1, 128, 256, 128, "fp16", seed=44)
+    q, k, v = workloads.make_inputs(w)
+    o, lse = sdp.sdp_fwd(q.cuda(), k.cuda(), v.cuda(), return_lse=False)
+    assert lse is None
+    ref_o, _ = oracle.sdp_fwd(q, k, v, oracle.FP16, w.shape, w.softmax_scale)
+    st = compare(o, None, ref_o, None, "fp16")
+    assert_within(st, "fp16")
+
+
+def test_default_scale_is_inverse_sqrt_d():
+    w = Workload("defscale", 1, 2, 1, 64, 64, 256, "fp16", seed=45)
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    o1, _ = sdp.sdp_fwd(q, k, v)
+    o2, _ = sdp.sdp_fwd(q, k, v, scale=1.0 / math.sqrt(256))
+    assert torch.equal(o1, o2)
