@@ -157,9 +157,9 @@ class ClockSampler:
 
 
 def cpu_rows_auto(w):
-    # about 10-20 s of oracle work on a 16-core host at ~1 fp64 GFLOP/s per core
+    # about 10-20 s of oracle work on a 16-core host (the oracle runs near 60 fp64 GFLOP/s there)
     per_row = 4.0 * w.Skv * w.D
-    target = 1.5e11
+    target = 8e11
     return int(max(2, min(w.Sq, target / (per_row * w.B * w.Hq))))
 
 
