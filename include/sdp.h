@@ -67,6 +67,42 @@ int sdp_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
             void *stream);
 
 /*
+ * sdp_fwd_noalloc — sdp_fwd for callers that cannot allocate device memory.
+ * The paper has no counterpart: this is a library-usage variant, not a step of
+ * the method.
+ *
+ * sdp_fwd allocates a 4-byte status word on a device the first time it runs
+ * there (cudaMalloc). Callers that cannot allow that use this entry point
+ * instead: code running inside a memory pool or arena that owns all device
+ * memory of the process, plugins whose host forbids allocations outside its
+ * own allocator, and code paths where an allocation's implicit
+ * synchronisation is not acceptable. This call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Arguments, layout, ownership, validation and results are exactly those of
+ * sdp_fwd, and it launches the same kernel. The kernel's only scratch, its
+ * status word, lives in a static device array of SDP_NOALLOC_SCRATCH_BYTES
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits. A launch needs 4 bytes of it whatever the problem size; a
+ * call needing more than the array holds would return SDP_ERR_OVERFLOW.
+ *
+ * Set-up: the first call on each device (made with that device current)
+ * looks up the device address of the array with cudaGetSymbolAddress and
+ * caches it; make that first call before any stream capture.
+ *
+ * Sharing: every call in the process uses the same array. Each call clears
+ * the status word on `stream` before its kernel, so calls that overlap on the
+ * GPU (different streams without ordering between them) race on it. A wait
+ * timeout inside this call (2 s per wait) leaves the affected output tile
+ * unwritten and is recorded only in that shared word: sdp_poll_status does
+ * not report it.
+ */
+#define SDP_NOALLOC_SCRATCH_BYTES 256
+int sdp_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                    int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale, int dtype,
+                    void *stream);
+
+/*
  * sdp_poll_status — synchronise `stream`, then read and clear the current
  * device's status word. Returns SDP_OK, SDP_ERR_DEVICE_TIMEOUT (a kernel
  * abandoned a wait after the timeout and returned without writing its
