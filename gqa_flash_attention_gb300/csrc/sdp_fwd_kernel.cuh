@@ -9,16 +9,22 @@
 // diagram": 16-bit operands into the contractions, fp32 softmax, output
 // rounded to the input type at the very end).
 //
-// Warp roles (192 threads):
+// Warp roles (256 threads):
 //   warps 0-3  softmax, lazy O rescale, epilogue. Thread t owns query row t,
 //              which is TMEM lane t (warp w may only touch lanes 32w..32w+31).
 //   warp 4     TMA producer: Q once, then K/V chunks through a ring of
 //              32 KB shared-memory slots (full/empty mbarriers).
-//   warp 5     tcgen05 MMA issuer (one thread) and TMEM owner.
+//   warp 5     TMEM owner and issuer of S_j = Q K_j^T (SMEM x SMEM -> TMEM fp32).
+//   warp 6     issuer of O += P_j V_j (P from TMEM, V from SMEM).
+//   warp 7     idle.
+// The tensor queue is shallow, so a single issuing thread that waits on a
+// barrier leaves the pipe idle; with two issuers one's waits are filled by
+// the other's MMAs. The two MMA streams are ordered only where they share
+// tensor memory: S_j overwrites the buffer that held P_{j-NSBUF}, so its
+// issuer first waits for PV_{j-NSBUF} to complete.
 //
-// Per KV tile j the tensor core runs S_j = Q K_j^T (SMEM x SMEM -> TMEM fp32)
-// and O += P_j V_j (P from TMEM, V from SMEM). S is double-buffered in TMEM so
-// that S_{j+1} is computed while the softmax of tile j runs; P_j overwrites
+// S has NSBUF tensor-memory buffers (2 at D=256, 3 at D=128), so the scores of
+// the next tiles are computed while the softmax of tile j runs; P_j overwrites
 // the first 64 columns of S_j's buffer as packed 16-bit pairs.
 //
 // Every mbarrier wait is bounded: after the timeout the waiting thread
@@ -34,7 +40,6 @@
 
 namespace sdp {
 
-
 enum : uint32_t {
     SITE_Q_FULL = 1,
     SITE_SLOT_EMPTY = 2,
@@ -45,6 +50,8 @@ enum : uint32_t {
 };
 
 constexpr int DEBUG_NO_LOADS = 1;
+constexpr int NUM_THREADS = 256;
+constexpr int O_DONE_RING = 4;  // PV completion barriers, used round robin
 
 template <int D>
 struct Layout {
@@ -57,6 +64,8 @@ struct Layout {
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int SMEM_LIMIT = 227 * 1024;
     static constexpr int NSLOTS = (SMEM_LIMIT - 2048 - Q_BYTES) / CHUNK_BYTES;
+    static constexpr int NSBUF = (D == 128) ? 3 : 2;      // S/P buffers in tensor memory
+    static constexpr int NBARS = 1 + 2 * NSLOTS + 2 * NSBUF + O_DONE_RING + 2;
     static constexpr int BAR_OFF = Q_BYTES + NSLOTS * CHUNK_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // barriers, then slack to align the base to 1 KB
     static constexpr int TM_O = 0;                           // O accumulator: columns [0, D)
@@ -65,8 +74,17 @@ struct Layout {
     static_assert(D == 128 || D == 256, "head dim");
     static_assert(NSLOTS >= 2, "ring");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
-    static_assert(D + 2 * BN <= TMEM_COLS, "tensor memory");
-    static_assert(8 * (2 * NSLOTS + 7) + 8 <= 256, "barrier area");
+    static_assert(D + NSBUF * BN <= TMEM_COLS, "tensor memory");
+    static_assert(8 * NBARS + 8 <= 256, "barrier area");
+    static_assert(O_DONE_RING >= NSBUF + 1, "PV completion ring must outrun the S buffers");
+    // An issuer waiting on the chunk at load position P reads slot P % NSLOTS by
+    // parity, which is only sound if the chunk at P - NSLOTS has landed. The
+    // S issuer at K_t has seen PV_{t-NSBUF} complete and every earlier K, so the
+    // only chunks before K_t that may still be in flight belong to V_{t-2}
+    // (NSBUF = 3); the PV issuer at V_j has seen S_j, so only K_{j+1} may be in
+    // flight. Neither sits exactly NSLOTS before the waited chunk when
+    // NSLOTS >= 2 * CHUNKS_PER_TILE and NSBUF <= 3.
+    static_assert(NSLOTS >= 2 * CHUNKS_PER_TILE && NSBUF <= 3, "ring parity soundness");
 };
 
 // Lazy rescale threshold in base-2 units: the running maximum is only moved
@@ -83,8 +101,8 @@ struct WaitCtx {
 // Slow path of wait_bounded: poll until the phase completes, the CTA aborts,
 // or the timeout passes (then raise the abort flag and record `site` and the
 // CTA index in the status word).
-static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned int *status,
-                                       unsigned long long timeout_ns, uint32_t site)
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              unsigned int *status, unsigned long long timeout_ns, uint32_t site)
 {
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -142,14 +160,31 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// Position of a chunk in the load order K_0, then for j = 0..n-1: K_{j+1} (if
+// any), V_j. Tiles are CPT chunks long; the producer and both issuers derive
+// ring slot = pos % NSLOTS and phase = (pos / NSLOTS) & 1 from it. Every
+// chunk's consumption depends only on chunks earlier in this order, so the
+// producer's in-order refill cannot deadlock.
+template <int CPT>
+__device__ __forceinline__ int pos_k(int t)
+{
+    return t == 0 ? 0 : CPT * (2 * t - 1);
+}
+template <int CPT>
+__device__ __forceinline__ int pos_v(int j, int n)
+{
+    return j == n - 1 ? CPT * (2 * j + 1) : CPT * (2 * j + 2);
+}
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     sdp_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    const KernelParams p)
 {
     using L = Layout<D>;
     constexpr int NS = L::NSLOTS;
+    constexpr int NB = L::NSBUF;
     constexpr int CPT = L::CHUNKS_PER_TILE;
     constexpr uint32_t IDESC_S = ptx::idesc_f16_f32acc(128, L::BN, BF16, false);  // Q (K-major) x K (K-major)
     constexpr uint32_t IDESC_PV = ptx::idesc_f16_f32acc(128, 128, BF16, true);    // P (TMEM) x V (N-major)
@@ -166,10 +201,10 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t slot_full0 = bar0 + 8u;
     const uint32_t slot_empty0 = bar0 + 8u * (1 + NS);
     const uint32_t s_full0 = bar0 + 8u * (1 + 2 * NS);
-    const uint32_t p_full0 = bar0 + 8u * (3 + 2 * NS);
-    const uint32_t o_done = bar0 + 8u * (5 + 2 * NS);
-    const uint32_t final_bar = bar0 + 8u * (6 + 2 * NS);
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * (7 + 2 * NS));
+    const uint32_t p_full0 = bar0 + 8u * (1 + 2 * NS + NB);
+    const uint32_t o_done0 = bar0 + 8u * (1 + 2 * NS + 2 * NB);
+    const uint32_t final0 = bar0 + 8u * (1 + 2 * NS + 2 * NB + O_DONE_RING);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -195,12 +230,14 @@ __global__ void __launch_bounds__(192, 1)
             ptx::mbar_init(slot_full0 + 8u * s, 1);
             ptx::mbar_init(slot_empty0 + 8u * s, 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NB; ++i) {
             ptx::mbar_init(s_full0 + 8u * i, 1);
             ptx::mbar_init(p_full0 + 8u * i, 128);
         }
-        ptx::mbar_init(o_done, 1);
-        ptx::mbar_init(final_bar, 1);
+        for (int i = 0; i < O_DONE_RING; ++i)
+            ptx::mbar_init(o_done0 + 8u * i, 1);
+        ptx::mbar_init(final0, 1);
+        ptx::mbar_init(final0 + 8u, 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -232,7 +269,6 @@ __global__ void __launch_bounds__(192, 1)
                 for (int c = 0; c < D / L::BOX_COLS; ++c)
                     ptx::tma_load_3d(s_q + c * L::BOX_BYTES, &tm_q, q_full, c * L::BOX_COLS, q0, z_q);
                 q_armed = true;
-                // Load order = MMA consumption order: K_0, then per j: K_{j+1}, V_j.
                 auto load_tile = [&](const CUtensorMap *map, int j) -> bool {
 #pragma unroll
                     for (int ch = 0; ch < CPT; ++ch) {
@@ -268,79 +304,85 @@ __global__ void __launch_bounds__(192, 1)
                     wait_drain(slot_full0 + 8u * s, (armed_par >> s) & 1u, p.timeout_ns);
         }
     } else if (warp == 5) {
-        // ------------------------------------------------------ MMA issuer
+        // ------------------------------------------- S = Q K^T issuer (1 thread)
         if (lane == 0) {
-            int slot = 0;
-            uint32_t ph = 0;
+            const uint64_t dq = ptx::smem_desc_sw128(s_q, 16, 1024);
+            const uint64_t dk = ptx::smem_desc_sw128(s_ring, 16, 1024);
             bool issued = false;
-            auto advance = [&]() {
-                if (++slot == NS) {
-                    slot = 0;
-                    ph ^= 1u;
-                }
-            };
-            // S_j = Q K_j^T into S buffer j&1; K-steps of 16 along D.
-            auto issue_s = [&](int j) -> bool {
-                const uint32_t d_tmem = tmem + L::TM_S + (j & 1) * L::BN;
-#pragma unroll
-                for (int ch = 0; ch < CPT; ++ch) {
-                    if (!wait_bounded(slot_full0 + 8u * slot, ph, cx, SITE_SLOT_FULL))
-                        return false;
-                    ptx::tc_fence_after();
-                    const uint32_t kbase = s_ring + slot * L::CHUNK_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t box = kk >> 2, off = (kk & 3) * 32;
-                        const uint64_t ad = ptx::smem_desc_sw128(s_q + (2 * ch + box) * L::BOX_BYTES + off, 16, 1024);
-                        const uint64_t bd = ptx::smem_desc_sw128(kbase + box * L::BOX_BYTES + off, 16, 1024);
-                        ptx::mma_ss(d_tmem, ad, bd, IDESC_S, (ch | kk) != 0);
-                    }
-                    issued = true;
-                    ptx::mma_commit(slot_empty0 + 8u * slot);
-                    advance();
-                }
-                ptx::mma_commit(s_full0 + 8u * (j & 1));
-                return true;
-            };
-            // O[:, 128ch : 128ch+128] += P_j V_j[:, 128ch : 128ch+128]; K-steps of 16 keys.
-            auto issue_pv = [&](int j) -> bool {
-                const uint32_t a_tmem = tmem + L::TM_S + (j & 1) * L::BN;
-#pragma unroll
-                for (int ch = 0; ch < CPT; ++ch) {
-                    if (!wait_bounded(slot_full0 + 8u * slot, ph, cx, SITE_SLOT_FULL))
-                        return false;
-                    ptx::tc_fence_after();
-                    const uint32_t vbase = s_ring + slot * L::CHUNK_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t bd = ptx::smem_desc_sw128(vbase + kk * 2048, L::BOX_BYTES, 1024);
-                        ptx::mma_ts(tmem + L::TM_O + ch * 128, a_tmem + kk * 8, bd, IDESC_PV, (j > 0) || (kk > 0));
-                    }
-                    issued = true;
-                    ptx::mma_commit(slot_empty0 + 8u * slot);
-                    advance();
-                }
-                ptx::mma_commit(o_done);
-                return true;
-            };
-
             bool ok = wait_bounded(q_full, 0, cx, SITE_Q_FULL);
-            if (ok)
-                ok = issue_s(0);
-            for (int j = 0; ok && j < n; ++j) {
-                if (j + 1 < n && !(ok = issue_s(j + 1)))
+            for (int t = 0; ok && t < n; ++t) {
+                if (t >= NB) {  // buffer t % NB held P_{t-NB}: PV_{t-NB} must have read it
+                    const int pv = t - NB;
+                    ok = wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx, SITE_O_DONE);
+                    if (!ok)
+                        break;
+                }
+                const uint32_t d_tmem = tmem + L::TM_S + (t % NB) * L::BN;
+                const int p0 = pos_k<CPT>(t);
+#pragma unroll
+                for (int ch = 0; ch < CPT; ++ch) {
+                    const int pos = p0 + ch;
+                    const int slot = pos % NS;
+                    if (!(ok = wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL)))
+                        break;
+                    ptx::tc_fence_after();
+                    const uint64_t kslot = dk + static_cast<uint64_t>((slot * L::CHUNK_BYTES) >> 4);
+                    const uint64_t qch = dq + static_cast<uint64_t>((2 * ch * L::BOX_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = ((kk >> 2) * L::BOX_BYTES + (kk & 3) * 32) >> 4;
+                        ptx::mma_ss(d_tmem, qch + off, kslot + off, IDESC_S, (ch | kk) != 0);
+                    }
+                    issued = true;
+                    ptx::mma_commit(slot_empty0 + 8u * slot);
+                }
+                if (!ok)
                     break;
-                if (!(ok = wait_bounded(p_full0 + 8u * (j & 1), (j >> 1) & 1, cx, SITE_P_FULL)))
-                    break;
-                ptx::tc_fence_after();
-                ok = issue_pv(j);
+                ptx::mma_commit(s_full0 + 8u * (t % NB));
             }
-            if (issued) {  // all MMAs complete before TMEM is freed
-                ptx::mma_commit(final_bar);
-                wait_drain(final_bar, 0, p.timeout_ns);
+            if (issued) {  // all of this thread's MMAs complete before TMEM is freed
+                ptx::mma_commit(final0);
+                wait_drain(final0, 0, p.timeout_ns);
             }
         }
-    } else {
+    } else if (warp == 6) {
+        // ------------------------------------------ O += P V issuer (1 thread)
+        if (lane == 0) {
+            const uint64_t dv = ptx::smem_desc_sw128(s_ring, L::BOX_BYTES, 1024);
+            bool issued = false;
+            bool ok = true;
+            for (int j = 0; ok && j < n; ++j) {
+                const int buf = j % NB;
+                if (!(ok = wait_bounded(p_full0 + 8u * buf, (j / NB) & 1, cx, SITE_P_FULL)))
+                    break;
+                ptx::tc_fence_after();
+                const uint32_t a_tmem = tmem + L::TM_S + buf * L::BN;
+                const int p0 = pos_v<CPT>(j, n);
+#pragma unroll
+                for (int ch = 0; ch < CPT; ++ch) {
+                    const int pos = p0 + ch;
+                    const int slot = pos % NS;
+                    if (!(ok = wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL)))
+                        break;
+                    ptx::tc_fence_after();
+                    const uint64_t vslot = dv + static_cast<uint64_t>((slot * L::CHUNK_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        ptx::mma_ts(tmem + L::TM_O + ch * 128, a_tmem + kk * 8, vslot + ((kk * 2048) >> 4), IDESC_PV,
+                                    (j > 0) || (kk > 0));
+                    issued = true;
+                    ptx::mma_commit(slot_empty0 + 8u * slot);
+                }
+                if (!ok)
+                    break;
+                ptx::mma_commit(o_done0 + 8u * (j % O_DONE_RING));
+            }
+            if (issued) {
+                ptx::mma_commit(final0 + 8u);
+                wait_drain(final0 + 8u, 0, p.timeout_ns);
+            }
+        }
+    } else if (warp < 4) {
         // --------------------------------------- softmax / correction / epilogue
         const int row = threadIdx.x;  // query row within the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
@@ -351,12 +393,13 @@ __global__ void __launch_bounds__(192, 1)
         bool ok = true;
 
         for (int j = 0; j < n; ++j) {
-            ok = wait_bounded(s_full0 + 8u * (j & 1), (j >> 1) & 1, cx, SITE_S_FULL);
+            const int buf = j % NB;
+            ok = wait_bounded(s_full0 + 8u * buf, (j / NB) & 1, cx, SITE_S_FULL);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok)
                 break;
             ptx::tc_fence_after();
-            const uint32_t ts = t_s + (j & 1) * L::BN;
+            const uint32_t ts = t_s + buf * L::BN;
             uint32_t sr[128];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -374,9 +417,8 @@ __global__ void __launch_bounds__(192, 1)
                     if (i >= valid)
                         s[i] = s[0];  // neutral for the max; weights zeroed below
             }
-            float mx0, mx1, mx2, mx3;
+            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
             if (c >= 0.f) {
-                mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
                 for (int i = 4; i < 128; i += 4) {
                     mx0 = fmaxf(mx0, s[i]);
@@ -386,7 +428,6 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 mx0 = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
             } else {
-                mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
                 for (int i = 4; i < 128; i += 4) {
                     mx0 = fminf(mx0, s[i]);
@@ -428,29 +469,31 @@ __global__ void __launch_bounds__(192, 1)
             const float tile_sum = (sum0 + sum1) + (sum2 + sum3);
             l = (j == 0) ? tile_sum : fmaf(l, alpha, tile_sum);
 
-            if (j > 0) {
-                // O must hold PV_{j-1} before it is rescaled and PV_j accumulates on it.
-                ok = wait_bounded(o_done, (j - 1) & 1, cx, SITE_O_DONE);
+            // Rescale O only in warps where some row's maximum moved; only they
+            // wait for PV_{j-1}. The skipped waits cannot alias: S_j completing
+            // implies PV_{j-NSBUF} completed, so the barrier that holds PV_{j-1}
+            // is at most one phase away (O_DONE_RING >= NSBUF + 1).
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                const int pv = j - 1;
+                ok = wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx, SITE_O_DONE);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok)
                     break;
                 ptx::tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        ptx::tmem_ld32(t_o + 32 * cc, o);
-                        ptx::tmem_wait_ld();
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(t_o + 32 * cc, o);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        ptx::tmem_st32(t_o + 32 * cc, o);
-                    }
-                    ptx::tmem_wait_st();
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    ptx::tmem_st32(t_o + 32 * cc, o);
                 }
+                ptx::tmem_wait_st();
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(p_full0 + 8u * (j & 1));
+            ptx::mbar_arrive(p_full0 + 8u * buf);
             m_used = m_new;
         }
 
@@ -458,7 +501,8 @@ __global__ void __launch_bounds__(192, 1)
         ptx::named_bar_sync(1, 128);
         ok = ok && !*abort_flag;
         if (ok) {
-            ok = wait_bounded(o_done, (n - 1) & 1, cx, SITE_O_DONE);
+            const int pv = n - 1;
+            ok = wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx, SITE_O_DONE);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
@@ -514,7 +558,7 @@ cudaError_t launch_sdp_fwd(const CUtensorMap &q, const CUtensorMap &k, const CUt
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::SMEM_BYTES);
     if (e != cudaSuccess)
         return e;
-    kern<<<grid, 192, Layout<D>::SMEM_BYTES, stream>>>(q, k, v, o, p);
+    kern<<<grid, NUM_THREADS, Layout<D>::SMEM_BYTES, stream>>>(q, k, v, o, p);
     return cudaGetLastError();
 }
 
