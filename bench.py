@@ -210,6 +210,13 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+def kernel_name(w):
+    """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
+    the units of each (batch, KV head) pair up, else the single-CTA kernel."""
+    n_qtiles = (w.Sq + 127) // 128
+    return "sdp_fwd_pair_kernel" if (n_qtiles * (w.Hq // w.Hkv)) % 2 == 0 else "sdp_fwd_kernel"
+
+
 def config_of(w, n):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv, "D": w.D,
             "io_dtype": w.dtype, "scale": w.softmax_scale, "causal": False, "peaky_k": w.peaky_k,
@@ -313,7 +320,7 @@ def ours_arm(args, w):
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": load_traffic(w.name),
                 "peak_source": f"{peak_src} bf16 dense (burst); fp16 runs at the same tensor rate",
-                "frac_of_sustained": achieved / peak_sus, "kernel": "sdp_fwd_kernel",
+                "frac_of_sustained": achieved / peak_sus, "kernel": kernel_name(w),
                 "launch_ms_median": statistics.median(per_launch_ms)}
 
     cpu = None

@@ -82,9 +82,10 @@ int device_state(int dev, unsigned int **status)
     return SDP_OK;
 }
 
-// 3-D map over a [planes, rows, D] 16-bit tensor; box = 64 columns x 128 rows x 1
-// plane with 128-byte swizzle. Rows past `rows` read as zero and are not written.
-int encode_map(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long planes)
+// 3-D map over a [planes, rows, D] 16-bit tensor; box = 64 columns x box_rows rows
+// x 1 plane with 128-byte swizzle. Rows past `rows` read as zero and are not written.
+int encode_map(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long planes,
+               unsigned box_rows = 128)
 {
     EncodeTiledFn enc = encoder();
     if (enc == nullptr)
@@ -92,7 +93,7 @@ int encode_map(CUtensorMap *map, const void *base, int dtype, int D, long long r
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(planes)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estride[3] = {1, 1, 1};
     CUresult r = enc(map, dtype == SDP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                      const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -145,11 +146,12 @@ int sdp_fwd(const void *q, const void *k, const void *v, void *o, float *lse, in
     if (rc != SDP_OK)
         return rc;
 
-    CUtensorMap mq, mk, mv, mo;
-    if ((rc = encode_map(&mq, q, dtype, D, Sq, planes_q)) != SDP_OK ||
-        (rc = encode_map(&mk, k, dtype, D, Skv, planes_kv)) != SDP_OK ||
-        (rc = encode_map(&mv, v, dtype, D, Skv, planes_kv)) != SDP_OK ||
-        (rc = encode_map(&mo, o, dtype, D, Sq, planes_q)) != SDP_OK)
+    sdp::LaunchMaps maps;
+    if ((rc = encode_map(&maps.q, q, dtype, D, Sq, planes_q)) != SDP_OK ||
+        (rc = encode_map(&maps.k, k, dtype, D, Skv, planes_kv)) != SDP_OK ||
+        (rc = encode_map(&maps.k_half, k, dtype, D, Skv, planes_kv, 64)) != SDP_OK ||
+        (rc = encode_map(&maps.v, v, dtype, D, Skv, planes_kv)) != SDP_OK ||
+        (rc = encode_map(&maps.o, o, dtype, D, Sq, planes_q)) != SDP_OK)
         return rc;
 
     sdp::KernelParams p{};
@@ -169,11 +171,9 @@ int sdp_fwd(const void *q, const void *k, const void *v, void *o, float *lse, in
     const int grid = static_cast<int>(units);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (D == 128)
-        e = dtype == SDP_BF16 ? sdp::launch_d128_bf16(mq, mk, mv, mo, p, grid, st)
-                              : sdp::launch_d128_fp16(mq, mk, mv, mo, p, grid, st);
+        e = dtype == SDP_BF16 ? sdp::launch_d128_bf16(maps, p, grid, st) : sdp::launch_d128_fp16(maps, p, grid, st);
     else
-        e = dtype == SDP_BF16 ? sdp::launch_d256_bf16(mq, mk, mv, mo, p, grid, st)
-                              : sdp::launch_d256_fp16(mq, mk, mv, mo, p, grid, st);
+        e = dtype == SDP_BF16 ? sdp::launch_d256_bf16(maps, p, grid, st) : sdp::launch_d256_fp16(maps, p, grid, st);
     if (e != cudaSuccess)
         return cuda_fail(e);
     return SDP_OK;

@@ -1,13 +1,14 @@
-// Instantiation of the attention forward kernel: head dim 256, fp16 I/O.
-#include "sdp_fwd_kernel.cuh"
+// Instantiation of the attention forward kernels: head dim 256, fp16 I/O.
+#include "sdp_fwd_pair.cuh"
 #include "sdp_launch.h"
 
 namespace sdp {
 
-cudaError_t launch_d256_fp16(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o,
-                             const KernelParams &p, int grid, cudaStream_t stream)
+cudaError_t launch_d256_fp16(const LaunchMaps &m, const KernelParams &p, int grid, cudaStream_t stream)
 {
-    return launch_sdp_fwd<256, false>(q, k, v, o, p, grid, stream);
+    if (use_pair(p, grid))
+        return launch_sdp_fwd_pair<256, false>(m.q, m.k_half, m.v, m.o, p, grid, stream);
+    return launch_sdp_fwd<256, false>(m.q, m.k, m.v, m.o, p, grid, stream);
 }
 
 }  // namespace sdp

@@ -18,9 +18,15 @@ struct KernelParams {
     int debug_flags;
 };
 
-#define SDP_DECLARE_LAUNCH(NAME)                                                                                  \
-    cudaError_t NAME(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o,       \
-                     const KernelParams &p, int grid, cudaStream_t stream);
+// Tensor maps of one launch: Q, K, V, O with 128-row boxes, and K with 64-row
+// boxes (half a KV tile) for the CTA-pair kernel.
+struct LaunchMaps {
+    CUtensorMap q, k, k_half, v, o;
+};
+
+// Launches the CTA-pair kernel when consecutive units pair up within one
+// (batch, KV head) and DEBUG_SINGLE_CTA is not set, else the single-CTA kernel.
+#define SDP_DECLARE_LAUNCH(NAME) cudaError_t NAME(const LaunchMaps &m, const KernelParams &p, int grid, cudaStream_t stream);
 
 SDP_DECLARE_LAUNCH(launch_d128_fp16)
 SDP_DECLARE_LAUNCH(launch_d128_bf16)

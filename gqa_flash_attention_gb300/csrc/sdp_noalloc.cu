@@ -82,12 +82,13 @@ int setup_device(int dev, unsigned int **scratch)
 }
 
 // Same view as sdp_fwd uses: [planes, rows, D], box 64 x 128 x 1, 128-byte swizzle.
-int encode(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long planes)
+int encode(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long planes,
+           unsigned box_rows = 128)
 {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(planes)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estride[3] = {1, 1, 1};
     CUresult r = g_encode(map, dtype == SDP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                           3, const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -136,9 +137,10 @@ extern "C" int sdp_fwd_noalloc(const void *q, const void *k, const void *v, void
     if (rc != SDP_OK)
         return rc;
 
-    CUtensorMap mq, mk, mv, mo;
-    if (encode(&mq, q, dtype, D, Sq, planes_q) != SDP_OK || encode(&mk, k, dtype, D, Skv, planes_kv) != SDP_OK ||
-        encode(&mv, v, dtype, D, Skv, planes_kv) != SDP_OK || encode(&mo, o, dtype, D, Sq, planes_q) != SDP_OK)
+    sdp::LaunchMaps maps;
+    if (encode(&maps.q, q, dtype, D, Sq, planes_q) != SDP_OK || encode(&maps.k, k, dtype, D, Skv, planes_kv) != SDP_OK ||
+        encode(&maps.k_half, k, dtype, D, Skv, planes_kv, 64) != SDP_OK ||
+        encode(&maps.v, v, dtype, D, Skv, planes_kv) != SDP_OK || encode(&maps.o, o, dtype, D, Sq, planes_q) != SDP_OK)
         return SDP_ERR_CUDA;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -163,10 +165,8 @@ extern "C" int sdp_fwd_noalloc(const void *q, const void *k, const void *v, void
     const int grid = static_cast<int>(units);
     cudaError_t e;
     if (D == 128)
-        e = dtype == SDP_BF16 ? sdp::launch_d128_bf16(mq, mk, mv, mo, p, grid, st)
-                              : sdp::launch_d128_fp16(mq, mk, mv, mo, p, grid, st);
+        e = dtype == SDP_BF16 ? sdp::launch_d128_bf16(maps, p, grid, st) : sdp::launch_d128_fp16(maps, p, grid, st);
     else
-        e = dtype == SDP_BF16 ? sdp::launch_d256_bf16(mq, mk, mv, mo, p, grid, st)
-                              : sdp::launch_d256_fp16(mq, mk, mv, mo, p, grid, st);
+        e = dtype == SDP_BF16 ? sdp::launch_d256_bf16(maps, p, grid, st) : sdp::launch_d256_fp16(maps, p, grid, st);
     return e == cudaSuccess ? SDP_OK : SDP_ERR_CUDA;
 }

@@ -70,7 +70,21 @@ for D in (128, 256):
 
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
 def test_small_cases_every_row(w):
+    # CTA-pair kernel wherever units pair within a KV group, else the single-CTA kernel
     check_full(w)
+
+
+DEBUG_SINGLE_CTA = 2
+
+
+@pytest.mark.parametrize("w", [w for w in SMALL if not w.name.startswith("one_")], ids=lambda w: w.name)
+def test_single_cta_kernel_every_row(w):
+    """The single-CTA kernel (used when units cannot pair) on the same cases."""
+    old = sdp.set_debug_flags(DEBUG_SINGLE_CTA)
+    try:
+        check_full(w)
+    finally:
+        sdp.set_debug_flags(old)
 
 
 def test_smallest_workload_every_row():
