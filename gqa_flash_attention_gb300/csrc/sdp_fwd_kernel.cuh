@@ -260,26 +260,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 4) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        {  // whole warp; one elected lane issues
             int slot = 0;
             uint32_t ph = 0, armed_mask = 0, armed_par = 0;
             bool q_armed = false;
             if (!(p.debug_flags & DEBUG_NO_LOADS)) {
-                ptx::mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+                ptx::mbar_arrive_expect_tx_w(q_full, L::Q_BYTES);
 #pragma unroll
                 for (int c = 0; c < D / L::BOX_COLS; ++c)
-                    ptx::tma_load_3d(s_q + c * L::BOX_BYTES, &tm_q, q_full, c * L::BOX_COLS, q0, z_q);
+                    ptx::tma_load_3d_w(s_q + c * L::BOX_BYTES, &tm_q, q_full, c * L::BOX_COLS, q0, z_q);
                 q_armed = true;
                 auto load_tile = [&](const CUtensorMap *map, int j) -> bool {
 #pragma unroll
                     for (int ch = 0; ch < CPT; ++ch) {
                         const uint32_t full = slot_full0 + 8u * slot;
-                        if (!wait_bounded(slot_empty0 + 8u * slot, ph ^ 1u, cx, SITE_SLOT_EMPTY))
+                        const bool ok = wait_bounded(slot_empty0 + 8u * slot, ph ^ 1u, cx, SITE_SLOT_EMPTY);
+                        if (!__all_sync(0xffffffffu, ok))
                             return false;
-                        ptx::mbar_arrive_expect_tx(full, L::CHUNK_BYTES);
+                        ptx::mbar_arrive_expect_tx_w(full, L::CHUNK_BYTES);
                         const uint32_t dst = s_ring + slot * L::CHUNK_BYTES;
-                        ptx::tma_load_3d(dst, map, full, ch * 128, j * L::BN, z_kv);
-                        ptx::tma_load_3d(dst + L::BOX_BYTES, map, full, ch * 128 + L::BOX_COLS, j * L::BN, z_kv);
+                        ptx::tma_load_3d_w(dst, map, full, ch * 128, j * L::BN, z_kv);
+                        ptx::tma_load_3d_w(dst + L::BOX_BYTES, map, full, ch * 128 + L::BOX_COLS, j * L::BN, z_kv);
                         armed_mask |= 1u << slot;
                         armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
                         if (++slot == NS) {
@@ -306,15 +307,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 5) {
         // ------------------------------------------- S = Q K^T issuer (1 thread)
-        if (lane == 0) {
+        {  // whole warp; one elected lane issues
             const uint64_t dq = ptx::smem_desc_sw128(s_q, 16, 1024);
             const uint64_t dk = ptx::smem_desc_sw128(s_ring, 16, 1024);
             bool issued = false;
-            bool ok = wait_bounded(q_full, 0, cx, SITE_Q_FULL);
+            bool ok = __all_sync(0xffffffffu, wait_bounded(q_full, 0, cx, SITE_Q_FULL));
             for (int t = 0; ok && t < n; ++t) {
                 if (t >= NB) {  // buffer t % NB held P_{t-NB}: PV_{t-NB} must have read it
                     const int pv = t - NB;
-                    ok = wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx, SITE_O_DONE);
+                    ok = __all_sync(0xffffffffu, wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx,
+                                                              SITE_O_DONE));
                     if (!ok)
                         break;
                 }
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int ch = 0; ch < CPT; ++ch) {
                     const int pos = p0 + ch;
                     const int slot = pos % NS;
-                    if (!(ok = wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL)))
+                    if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
                         break;
                     ptx::tc_fence_after();
                     const uint64_t kslot = dk + static_cast<uint64_t>((slot * L::CHUNK_BYTES) >> 4);
@@ -332,29 +334,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = ((kk >> 2) * L::BOX_BYTES + (kk & 3) * 32) >> 4;
-                        ptx::mma_ss(d_tmem, qch + off, kslot + off, IDESC_S, (ch | kk) != 0);
+                        ptx::mma_ss_w(d_tmem, qch + off, kslot + off, IDESC_S, (ch | kk) != 0);
                     }
                     issued = true;
-                    ptx::mma_commit(slot_empty0 + 8u * slot);
+                    ptx::mma_commit_w(slot_empty0 + 8u * slot);
                 }
                 if (!ok)
                     break;
-                ptx::mma_commit(s_full0 + 8u * (t % NB));
+                ptx::mma_commit_w(s_full0 + 8u * (t % NB));
             }
             if (issued) {  // all of this thread's MMAs complete before TMEM is freed
-                ptx::mma_commit(final0);
+                ptx::mma_commit_w(final0);
                 wait_drain(final0, 0, p.timeout_ns);
             }
         }
     } else if (warp == 6) {
         // ------------------------------------------ O += P V issuer (1 thread)
-        if (lane == 0) {
+        {  // whole warp; one elected lane issues
             const uint64_t dv = ptx::smem_desc_sw128(s_ring, L::BOX_BYTES, 1024);
             bool issued = false;
             bool ok = true;
             for (int j = 0; ok && j < n; ++j) {
                 const int buf = j % NB;
-                if (!(ok = wait_bounded(p_full0 + 8u * buf, (j / NB) & 1, cx, SITE_P_FULL)))
+                if (!(ok = __all_sync(0xffffffffu, wait_bounded(p_full0 + 8u * buf, (j / NB) & 1, cx, SITE_P_FULL))))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t a_tmem = tmem + L::TM_S + buf * L::BN;
@@ -363,23 +365,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int ch = 0; ch < CPT; ++ch) {
                     const int pos = p0 + ch;
                     const int slot = pos % NS;
-                    if (!(ok = wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL)))
+                    if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
                         break;
                     ptx::tc_fence_after();
                     const uint64_t vslot = dv + static_cast<uint64_t>((slot * L::CHUNK_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        ptx::mma_ts(tmem + L::TM_O + ch * 128, a_tmem + kk * 8, vslot + ((kk * 2048) >> 4), IDESC_PV,
+                        ptx::mma_ts_w(tmem + L::TM_O + ch * 128, a_tmem + kk * 8, vslot + ((kk * 2048) >> 4), IDESC_PV,
                                     (j > 0) || (kk > 0));
                     issued = true;
-                    ptx::mma_commit(slot_empty0 + 8u * slot);
+                    ptx::mma_commit_w(slot_empty0 + 8u * slot);
                 }
                 if (!ok)
                     break;
-                ptx::mma_commit(o_done0 + 8u * (j % O_DONE_RING));
+                ptx::mma_commit_w(o_done0 + 8u * (j % O_DONE_RING));
             }
             if (issued) {
-                ptx::mma_commit(final0 + 8u);
+                ptx::mma_commit_w(final0 + 8u);
                 wait_drain(final0 + 8u, 0, p.timeout_ns);
             }
         }

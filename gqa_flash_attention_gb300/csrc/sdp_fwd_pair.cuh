@@ -174,20 +174,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 4) {
         // ------------------------------------------------- TMA producer (both CTAs)
-        if (lane == 0 && !(p.debug_flags & DEBUG_NO_LOADS)) {
+        if (!(p.debug_flags & DEBUG_NO_LOADS)) {  // whole warp; one elected lane issues
             const uint32_t q_full_l = ptx::map_to_rank(q_full, 0);
             if (leader)
-                ptx::mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
+                ptx::mbar_arrive_expect_tx_w(q_full, 2 * L::Q_BYTES);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-                ptx::tma_load_3d_pair(s_q + c * L::Q_BOX_BYTES, &tm_q, q_full_l, c * 64, q0, z_q);
+                ptx::tma_load_3d_pair_w(s_q + c * L::Q_BOX_BYTES, &tm_q, q_full_l, c * 64, q0, z_q);
             int slot = 0;
             uint32_t ph = 0;
             auto next_slot = [&](uint32_t &full_l, uint32_t &dst) -> bool {
-                if (!wait_bounded(slot_empty0 + 8u * slot, ph ^ 1u, cx, SITE_SLOT_EMPTY))
+                const bool ok = wait_bounded(slot_empty0 + 8u * slot, ph ^ 1u, cx, SITE_SLOT_EMPTY);
+                if (!__all_sync(0xffffffffu, ok))
                     return false;
                 if (leader)
-                    ptx::mbar_arrive_expect_tx(slot_full0 + 8u * slot, 2 * L::HALF_BYTES);
+                    ptx::mbar_arrive_expect_tx_w(slot_full0 + 8u * slot, 2 * L::HALF_BYTES);
                 full_l = ptx::map_to_rank(slot_full0 + 8u * slot, 0);
                 dst = s_ring + slot * L::HALF_BYTES;
                 if (++slot == NS) {
@@ -202,7 +203,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     return false;
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    ptx::tma_load_3d_pair(dst + c * L::K_BOX_BYTES, &tm_k, full_l, c * 64,
+                    ptx::tma_load_3d_pair_w(dst + c * L::K_BOX_BYTES, &tm_k, full_l, c * 64,
                                           j * L::BN + 64 * static_cast<int>(rank), z_kv);
                 return true;
             };
@@ -212,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     return false;
 #pragma unroll
                 for (int c = 0; c < D / 128; ++c)
-                    ptx::tma_load_3d_pair(dst + c * L::V_BOX_BYTES, &tm_v, full_l,
+                    ptx::tma_load_3d_pair_w(dst + c * L::V_BOX_BYTES, &tm_v, full_l,
                                           static_cast<int>(rank) * (D / 2) + c * 64, j * L::BN, z_kv);
                 return true;
             };
@@ -226,21 +227,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 5) {
         // ------------------------------------- S = Q K^T issuer (leader, 1 thread)
-        if (lane == 0 && leader) {
+        if (leader) {  // whole warp; one elected lane issues
             const uint64_t dq = ptx::smem_desc_sw128(s_q, 16, 1024);
             const uint64_t dk = ptx::smem_desc_sw128(s_ring, 16, 1024);
             bool issued = false;
-            bool ok = wait_bounded(q_full, 0, cx, SITE_Q_FULL);
+            bool ok = __all_sync(0xffffffffu, wait_bounded(q_full, 0, cx, SITE_Q_FULL));
             for (int t = 0; ok && t < n; ++t) {
                 if (t >= NB) {
                     const int pv = t - NB;
-                    ok = wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx, SITE_O_DONE);
+                    ok = __all_sync(0xffffffffu, wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx,
+                                                              SITE_O_DONE));
                     if (!ok)
                         break;
                 }
                 const int pos = pos_k<1>(t);
                 const int slot = pos % NS;
-                if (!(ok = wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL)))
+                if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + L::TM_S + (t % NB) * L::BN;
@@ -248,46 +250,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t box = kk >> 2, off = (kk & 3) * 32;
-                    ptx::mma_ss_pair(d_tmem, dq + ((box * L::Q_BOX_BYTES + off) >> 4),
+                    ptx::mma_ss_pair_w(d_tmem, dq + ((box * L::Q_BOX_BYTES + off) >> 4),
                                      kslot + ((box * L::K_BOX_BYTES + off) >> 4), IDESC_S, kk != 0);
                 }
                 issued = true;
-                ptx::mma_commit_pair(slot_empty0 + 8u * slot);
-                ptx::mma_commit_pair(s_full0 + 8u * (t % NB));
+                ptx::mma_commit_pair_w(slot_empty0 + 8u * slot);
+                ptx::mma_commit_pair_w(s_full0 + 8u * (t % NB));
             }
             if (issued) {
-                ptx::mma_commit_pair(final0);
+                ptx::mma_commit_pair_w(final0);
                 wait_drain(final0, 0, p.timeout_ns);
             }
         }
     } else if (warp == 6) {
         // ------------------------------------ O += P V issuer (leader, 1 thread)
-        if (lane == 0 && leader) {
+        if (leader) {  // whole warp; one elected lane issues
             const uint64_t dv = ptx::smem_desc_sw128(s_ring, L::V_BOX_BYTES, 1024);
             bool issued = false;
             bool ok = true;
             for (int j = 0; ok && j < n; ++j) {
                 const int buf = j % NB;
-                if (!(ok = wait_bounded(p_full0 + 8u * buf, (j / NB) & 1, cx, SITE_P_FULL)))
+                if (!(ok = __all_sync(0xffffffffu, wait_bounded(p_full0 + 8u * buf, (j / NB) & 1, cx, SITE_P_FULL))))
                     break;
                 ptx::tc_fence_after();
                 const int pos = pos_v<1>(j, n);
                 const int slot = pos % NS;
-                if (!(ok = wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL)))
+                if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t a_tmem = tmem + L::TM_S + buf * L::BN;
                 const uint64_t vslot = dv + static_cast<uint64_t>((slot * L::HALF_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    ptx::mma_ts_pair(tmem + L::TM_O, a_tmem + kk * 8, vslot + ((kk * 2048) >> 4), IDESC_PV,
+                    ptx::mma_ts_pair_w(tmem + L::TM_O, a_tmem + kk * 8, vslot + ((kk * 2048) >> 4), IDESC_PV,
                                      (j > 0) || (kk > 0));
                 issued = true;
-                ptx::mma_commit_pair(slot_empty0 + 8u * slot);
-                ptx::mma_commit_pair(o_done0 + 8u * (j % O_DONE_RING));
+                ptx::mma_commit_pair_w(slot_empty0 + 8u * slot);
+                ptx::mma_commit_pair_w(o_done0 + 8u * (j % O_DONE_RING));
             }
             if (issued) {
-                ptx::mma_commit_pair(final0 + 8u);
+                ptx::mma_commit_pair_w(final0 + 8u);
                 wait_drain(final0 + 8u, 0, p.timeout_ns);
             }
         }
