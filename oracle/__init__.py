@@ -49,9 +49,9 @@ def _load():
         lib = ctypes.CDLL(_LIB_PATH)
         p = ctypes.c_void_p
         i = ctypes.c_int
-        lib.oracle_sdp_fwd_rows.argtypes = [p, p, p, i, i, i, i, i, i, i, ctypes.c_double, p, i, p, p]
+        lib.oracle_sdp_fwd_rows.argtypes = [p, p, p, i, i, i, i, i, i, i, ctypes.c_double, i, p, i, p, p]
         lib.oracle_sdp_fwd_rows.restype = i
-        lib.oracle_sdp_row_probs.argtypes = [p, p, p, i, i, i, i, i, i, i, ctypes.c_double,
+        lib.oracle_sdp_row_probs.argtypes = [p, p, p, i, i, i, i, i, i, i, ctypes.c_double, i,
                                              i, i, i, p, p, p]
         lib.oracle_sdp_row_probs.restype = i
         lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
@@ -92,11 +92,12 @@ def bf16_to_double(bits: int) -> float:
     return float(_load().oracle_bf16_to_double(int(bits) & 0xFFFF))
 
 
-def sdp_fwd_rows(q, k, v, dtype: int, shape, scale: float, rows: np.ndarray):
+def sdp_fwd_rows(q, k, v, dtype: int, shape, scale: float, rows: np.ndarray, causal: bool = False):
     """O and LSE (fp64) of the query rows ``rows[b, h, :]`` of every (b, h).
 
     q: [B, Hq, Sq, D], k/v: [B, Hkv, Skv, D] 16-bit patterns (or fp16/bf16
     tensors). ``rows`` is int32 [B, Hq, n]. Returns (o [B, Hq, n, D], lse [B, Hq, n]).
+    With ``causal``, row i sees keys 0..i.
     """
     B, Hq, Hkv, Sq, Skv, D = (int(x) for x in shape)
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
@@ -107,20 +108,20 @@ def sdp_fwd_rows(q, k, v, dtype: int, shape, scale: float, rows: np.ndarray):
     o = np.empty((B, Hq, n, D), dtype=np.float64)
     lse = np.empty((B, Hq, n), dtype=np.float64)
     rc = _load().oracle_sdp_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), int(dtype), B, Hq, Hkv, Sq, Skv, D,
-                                     float(scale), _ptr(rows), n, _ptr(o), _ptr(lse))
+                                     float(scale), int(bool(causal)), _ptr(rows), n, _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle rejected the shape or row indices")
     return o, lse
 
 
-def sdp_fwd(q, k, v, dtype: int, shape, scale: float):
+def sdp_fwd(q, k, v, dtype: int, shape, scale: float, causal: bool = False):
     """O and LSE (fp64) of every query row."""
     B, Hq, _, Sq, _, _ = (int(x) for x in shape)
     rows = np.broadcast_to(np.arange(Sq, dtype=np.int32), (B, Hq, Sq))
-    return sdp_fwd_rows(q, k, v, dtype, shape, scale, rows)
+    return sdp_fwd_rows(q, k, v, dtype, shape, scale, rows, causal)
 
 
-def row_probs(q, k, v, dtype: int, shape, scale: float, b: int, h: int, i: int):
+def row_probs(q, k, v, dtype: int, shape, scale: float, b: int, h: int, i: int, causal: bool = False):
     """Softmax weights (fp64 [Skv]), O row and LSE of query row (b, h, i)."""
     B, Hq, Hkv, Sq, Skv, D = (int(x) for x in shape)
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
@@ -128,7 +129,8 @@ def row_probs(q, k, v, dtype: int, shape, scale: float, b: int, h: int, i: int):
     o = np.empty(D, dtype=np.float64)
     lse = np.empty(1, dtype=np.float64)
     rc = _load().oracle_sdp_row_probs(_ptr(qb), _ptr(kb), _ptr(vb), int(dtype), B, Hq, Hkv, Sq, Skv, D,
-                                      float(scale), int(b), int(h), int(i), _ptr(p), _ptr(o), _ptr(lse))
+                                      float(scale), int(bool(causal)), int(b), int(h), int(i), _ptr(p), _ptr(o),
+                                      _ptr(lse))
     if rc != 0:
         raise ValueError("oracle rejected the shape or row index")
     return p, o, float(lse[0])

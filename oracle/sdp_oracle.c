@@ -22,6 +22,12 @@
  *   O[b,h,i] = sum_j exp(s_j - M) * V[b,g,j,:] / L
  *   LSE      = M + ln L                  natural log, one value per (b,h,i)
  *
+ * Causal variant (causal != 0): row i sees keys j <= i only (top-left
+ * alignment, the convention of PyTorch's is_causal; the "SyclKittens" summary,
+ * sections E.4 and E.6, measures causal attention without fixing one). The
+ * maximum, sum and weighted sum then run over those keys; every row keeps
+ * at least key 0.
+ *
  * This is the result the single-pass online-softmax kernel of the
  * "xe2-sdp-hd256" page (section "HD=256 Architecture Differences") and the
  * "xe2-sdp-bf16" page (section "Data flow diagram") reaches up to rounding
@@ -91,6 +97,7 @@ static double decode(uint16_t bits, int dtype)
 static void attend_row(const double *q, const double *Kg, const double *Vg, int Skv, int D,
                        double scale, double *s, double *p, double *o, double *lse)
 {
+    /* Skv here is the number of keys this row sees (all keys, or i+1 when causal) */
     /* scores */
     for (int j = 0; j < Skv; ++j) {
         double acc = 0.0;
@@ -143,10 +150,11 @@ static int check_shape(int B, int Hq, int Hkv, int Sq, int Skv, int D, int dtype
  *         in (b, h) order; every index must lie in [0, Sq).
  * o_out:  double [B*Hq*nrows*D], O for those rows in the same order.
  * lse_out: double [B*Hq*nrows] (may be NULL).
+ * causal: 0 for full attention, nonzero for row i seeing keys 0..i.
  * Returns 0, or -1 on a bad shape or row index.
  */
 int oracle_sdp_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
-                        int B, int Hq, int Hkv, int Sq, int Skv, int D, double scale,
+                        int B, int Hq, int Hkv, int Sq, int Skv, int D, double scale, int causal,
                         const int32_t *rows, int nrows, double *o_out, double *lse_out)
 {
     if (check_shape(B, Hq, Hkv, Sq, Skv, D, dtype) || nrows < 0)
@@ -195,7 +203,8 @@ int oracle_sdp_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                     for (int d = 0; d < D; ++d)
                         qrow[d] = decode(q[q_off + d], dtype);
                     double lse;
-                    attend_row(qrow, Kg, Vg, Skv, D, scale, s, p, o_out + (size_t)slot * D, &lse);
+                    const int seen = (causal && i + 1 < Skv) ? i + 1 : Skv;
+                    attend_row(qrow, Kg, Vg, seen, D, scale, s, p, o_out + (size_t)slot * D, &lse);
                     if (lse_out)
                         lse_out[slot] = lse;
                 }
@@ -211,11 +220,12 @@ int oracle_sdp_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 }
 
 /*
- * The softmax weights of one query row (b, h, i): p_out double [Skv].
+ * The softmax weights of one query row (b, h, i): p_out double [Skv] (keys a
+ * causal row does not see get weight 0).
  * Exposed so that properties of the weights themselves can be checked.
  */
 int oracle_sdp_row_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
-                         int B, int Hq, int Hkv, int Sq, int Skv, int D, double scale,
+                         int B, int Hq, int Hkv, int Sq, int Skv, int D, double scale, int causal,
                          int b, int h, int i, double *p_out, double *o_out, double *lse_out)
 {
     if (check_shape(B, Hq, Hkv, Sq, Skv, D, dtype))
@@ -237,7 +247,10 @@ int oracle_sdp_row_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v
         }
         for (int d = 0; d < D; ++d)
             qrow[d] = decode(q[q_off + d], dtype);
-        attend_row(qrow, Kg, Vg, Skv, D, scale, s, p_out, o_out, lse_out);
+        const int seen = (causal && i + 1 < Skv) ? i + 1 : Skv;
+        for (int j = seen; j < Skv; ++j)
+            p_out[j] = 0.0;
+        attend_row(qrow, Kg, Vg, seen, D, scale, s, p_out, o_out, lse_out);
         status = 0;
     }
     free(Kg);

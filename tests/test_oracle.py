@@ -267,3 +267,56 @@ def test_rejects_bad_shapes():
     q, k, v = rand_qkv(1, 3, 1, 2, 2, 8, FP16, seed=1)
     with pytest.raises(ValueError):
         oracle.sdp_fwd_rows(q, k, v, FP16, (1, 3, 1, 2, 2, 8), 1.0, rows)
+
+
+# ------------------------------------------------------------------- causal
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,D", [
+    (1, 4, 1, 9, 9, 16),
+    (2, 4, 2, 13, 7, 32),   # more queries than keys: late rows see every key
+    (1, 2, 2, 5, 23, 8),    # more keys than queries: row i still sees keys 0..i only
+])
+def test_causal_matches_torch_float64_sdpa(dtype, B, Hq, Hkv, Sq, Skv, D):
+    """Top-left alignment: row i sees keys 0..i (torch's is_causal convention)."""
+    q, k, v = rand_qkv(B, Hq, Hkv, Sq, Skv, D, dtype, seed=Sq * 31 + Skv)
+    scale = 0.6 / math.sqrt(D)
+    o, lse = oracle.sdp_fwd(q, k, v, dtype, (B, Hq, Hkv, Sq, Skv, D), scale, causal=True)
+    G = Hq // Hkv
+    qd, kd, vd = q.double(), k.double().repeat_interleave(G, dim=1), v.double().repeat_interleave(G, dim=1)
+    ref = F.scaled_dot_product_attention(qd, kd, vd, scale=scale, is_causal=True)
+    s = qd @ kd.transpose(-1, -2) * scale
+    mask = torch.ones(Sq, Skv, dtype=torch.bool).tril()
+    ref_lse = torch.logsumexp(s.masked_fill(~mask, float("-inf")), dim=-1)
+    assert np.abs(o - ref.numpy()).max() <= 1e-12
+    assert np.abs(lse - ref_lse.numpy()).max() <= 1e-12
+
+
+def test_causal_first_row_is_first_value_row():
+    q, k, v = rand_qkv(1, 2, 1, 6, 40, 16, FP16, seed=61)
+    o, lse = oracle.sdp_fwd(q, k, v, FP16, (1, 2, 1, 6, 40, 16), 0.5, causal=True)
+    vd, qd, kd = v.double().numpy(), q.double().numpy(), k.double().numpy()
+    for h in range(2):
+        assert np.array_equal(o[0, h, 0], vd[0, 0, 0])
+        assert abs(lse[0, h, 0] - 0.5 * math.fsum(qd[0, h, 0] * kd[0, 0, 0])) <= 1e-12
+
+
+def test_causal_row_equals_full_attention_on_its_prefix():
+    shape = (1, 4, 2, 12, 12, 16)
+    q, k, v = rand_qkv(*shape, BF16, seed=62)
+    o, lse = oracle.sdp_fwd(q, k, v, BF16, shape, 0.3, causal=True)
+    for i in (0, 3, 11):
+        qi = q[:, :, i:i + 1].contiguous()
+        kp, vp = k[:, :, :i + 1].contiguous(), v[:, :, :i + 1].contiguous()
+        o2, l2 = oracle.sdp_fwd(qi, kp, vp, BF16, (1, 4, 2, 1, i + 1, 16), 0.3)
+        assert np.abs(o[:, :, i] - o2[:, :, 0]).max() <= 1e-13
+        assert np.abs(lse[:, :, i] - l2[:, :, 0]).max() <= 1e-13
+
+
+def test_causal_weights_vanish_past_the_diagonal():
+    shape = (1, 2, 1, 8, 8, 16)
+    q, k, v = rand_qkv(*shape, FP16, seed=63)
+    for i in range(8):
+        p, _, _ = oracle.row_probs(q, k, v, FP16, shape, 0.4, 0, 1, i, causal=True)
+        assert (p[i + 1:] == 0).all() and (p[:i + 1] > 0).all()
+        assert abs(p.sum() - 1.0) <= 1e-12
