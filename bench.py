@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.ALL_WORKLOADS))
     ap.add_argument("--cpu-rows", type=int, default=0, help="query rows per head in the CPU sample (0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -172,9 +172,10 @@ def run_cpu_oracle(w, rows_per_head, q=None, k=None, v=None):
     rows = workloads.sample_rows(w, rows_per_head, seed=1234)
     dt = oracle.FP16 if w.dtype == "fp16" else oracle.BF16
     t0 = time.perf_counter()
-    oracle.sdp_fwd_rows(q, k, v, dt, w.shape, w.softmax_scale, rows)
+    oracle.sdp_fwd_rows(q, k, v, dt, w.shape, w.softmax_scale, rows, causal=w.causal)
     sec = time.perf_counter() - t0
-    flops = 4.0 * w.B * w.Hq * rows.shape[2] * w.Skv * w.D
+    seen = (np.minimum(rows.astype(np.int64) + 1, w.Skv) if w.causal else np.full(rows.shape, w.Skv)).sum()
+    flops = 4.0 * float(seen) * w.D
     return flops / sec / 1e12, sec, rows.shape[2], oracle.num_threads()
 
 
@@ -212,14 +213,17 @@ def reference_arm(args, w):
 
 def kernel_name(w):
     """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
-    the units of each (batch, KV head) pair up, else the single-CTA kernel."""
+    the units of each (batch, KV head) pair up (and, causal, share the query
+    tile), else the single-CTA kernel."""
     n_qtiles = (w.Sq + 127) // 128
-    return "sdp_fwd_pair_kernel" if (n_qtiles * (w.Hq // w.Hkv)) % 2 == 0 else "sdp_fwd_kernel"
+    G = w.Hq // w.Hkv
+    pair = (n_qtiles * G) % 2 == 0 and not (w.causal and G % 2)
+    return "sdp_fwd_pair_kernel" if pair else "sdp_fwd_kernel"
 
 
 def config_of(w, n):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv, "D": w.D,
-            "io_dtype": w.dtype, "scale": w.softmax_scale, "causal": False, "peaky_k": w.peaky_k,
+            "io_dtype": w.dtype, "scale": w.softmax_scale, "causal": w.causal, "peaky_k": w.peaky_k,
             "flops_per_step_per_gpu": w.flops(), "l2": "inputs larger than L2 (Q and O exceed 126 MB); no flush",
             "parallelism": "replicas" if n > 1 else "single GPU"}
 
@@ -242,7 +246,7 @@ def ours_arm(args, w):
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
-        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse)
+        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse, causal=w.causal)
     torch.cuda.synchronize(dev)
     if sdp.poll_status() != sdp.SDP_OK:
         raise RuntimeError("kernel reported a timeout during warm-up")
@@ -256,7 +260,7 @@ def ours_arm(args, w):
     torch.cuda.synchronize(dev)
     ev[0].record(stream)
     for i in range(K):
-        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse)
+        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse, causal=w.causal)
         ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -286,7 +290,7 @@ def ours_arm(args, w):
             q.copy_(qp, non_blocking=True)
             k.copy_(kp, non_blocking=True)
             v.copy_(vp, non_blocking=True)
-            sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse)
+            sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse, causal=w.causal)
             op.copy_(o, non_blocking=True)
             lp.copy_(lse, non_blocking=True)
 
@@ -345,7 +349,7 @@ def ours_arm(args, w):
 
 def main():
     args = parse()
-    w = workloads.WORKLOADS[args.workload]
+    w = workloads.ALL_WORKLOADS[args.workload]
     if args.impl == "reference":
         reference_arm(args, w)
     else:

@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         L.sdp_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         L.sdp_fwd.restype = i
+        L.sdp_fwd_causal.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        L.sdp_fwd_causal.restype = i
         L.sdp_poll_status.argtypes = [vp]
         L.sdp_poll_status.restype = i
         L.sdp_last_status_detail.argtypes = []
@@ -94,17 +96,18 @@ def _stream_handle(stream, device) -> int:
 
 
 def sdp_fwd_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
-                scale: float, dtype: int, stream: int = 0) -> int:
-    """The raw C call with integer addresses; returns the status code."""
-    return int(lib().sdp_fwd(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.c_void_p(o),
+                scale: float, dtype: int, stream: int = 0, causal: bool = False) -> int:
+    """The raw C call (sdp_fwd, or sdp_fwd_causal) with integer addresses; returns the status code."""
+    fn = lib().sdp_fwd_causal if causal else lib().sdp_fwd
+    return int(fn(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.c_void_p(o),
                              ctypes.c_void_p(lse), int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(D),
                              ctypes.c_float(scale), int(dtype), ctypes.c_void_p(stream)))
 
 
 def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
             out: torch.Tensor | None = None, lse: torch.Tensor | None = None, return_lse: bool = True,
-            stream=None):
-    """Grouped-query attention forward on sm_103a.
+            stream=None, causal: bool = False):
+    """Grouped-query attention forward on sm_103a (causal: row i sees keys 0..i).
 
     q: [B, Hq, Sq, D]; k, v: [B, Hkv, Skv, D]; fp16 or bf16, contiguous, on one
     CUDA device; D in {128, 256}; Hq a multiple of Hkv. Returns (o, lse) with o
@@ -138,7 +141,7 @@ def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
     with torch.cuda.device(q.device):
         rc = sdp_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                          0 if lse is None else lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
-                         _DTYPE_CODE[q.dtype], _stream_handle(stream, q.device))
+                         _DTYPE_CODE[q.dtype], _stream_handle(stream, q.device), causal=causal)
     _check(rc)
     return out, lse
 

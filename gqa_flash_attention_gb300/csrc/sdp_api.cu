@@ -108,10 +108,10 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-int sdp_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
-            int Skv, int D, float scale, int dtype, void *stream)
+int forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
+            int Skv, int D, float scale, int dtype, int causal, void *stream)
 {
     // ---- validation: no CUDA call happens before all of it passes
     if (dtype != SDP_FP16 && dtype != SDP_BF16)
@@ -167,6 +167,7 @@ int sdp_fwd(const void *q, const void *k, const void *v, void *o, float *lse, in
     p.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);  // scale * log2(e)
     p.timeout_ns = static_cast<unsigned long long>(g_timeout_ms.load()) * 1000000ull;
     p.debug_flags = g_debug_flags.load();
+    p.causal = causal ? 1 : 0;
 
     const int grid = static_cast<int>(units);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -177,6 +178,22 @@ int sdp_fwd(const void *q, const void *k, const void *v, void *o, float *lse, in
     if (e != cudaSuccess)
         return cuda_fail(e);
     return SDP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sdp_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
+            int Skv, int D, float scale, int dtype, void *stream)
+{
+    return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, dtype, 0, stream);
+}
+
+int sdp_fwd_causal(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
+                   int Skv, int D, float scale, int dtype, void *stream)
+{
+    return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, dtype, 1, stream);
 }
 
 int sdp_poll_status(void *stream)
@@ -239,7 +256,7 @@ const char *sdp_strerror(int code)
     }
 }
 
-int sdp_version(void) { return 100; }
+int sdp_version(void) { return 101; }
 
 void sdp_shutdown(void)
 {

@@ -216,14 +216,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int u = blockIdx.x;
     const int hi = u % p.G;
     u /= p.G;
-    const int qt = u % p.n_qtiles;
+    // Causal units do qt + 1 tiles: start the longest ones first.
+    const int qt = p.causal ? p.n_qtiles - 1 - (u % p.n_qtiles) : (u % p.n_qtiles);
     const int bg = u / p.n_qtiles;  // b * Hkv + g
     const int b = bg / p.Hkv;
     const int g = bg - b * p.Hkv;
     const int z_q = b * p.Hq + g * p.G + hi;  // (b, h) plane of Q, O and LSE
     const int z_kv = bg;                      // (b, g) plane of K and V
     const int q0 = qt * L::BM;
-    const int n = p.n_kvtiles;
+    // Tiles this unit reads: all of them, or (causal) those holding keys <= its last row.
+    const int n = p.causal ? min(p.n_kvtiles, qt + 1) : p.n_kvtiles;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
@@ -413,7 +415,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int i = 0; i < 128; ++i)
                 s[i] = __uint_as_float(sr[i]);
 
-            const int valid = p.Skv - j * L::BN;  // >= 1
+            // keys of this tile the row sees (>= 1): all < Skv, and (causal) <= the row itself
+            const int valid = (p.causal ? min(p.Skv, q0 + row + 1) : p.Skv) - j * L::BN;  // >= 1
             if (valid < L::BN) {
 #pragma unroll
                 for (int i = 1; i < 128; ++i)

@@ -129,14 +129,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     int u = blockIdx.x;
     const int hi = u % p.G;
     u /= p.G;
-    const int qt = u % p.n_qtiles;
+    // Causal units do qt + 1 tiles: start the longest ones first.
+    const int qt = p.causal ? p.n_qtiles - 1 - (u % p.n_qtiles) : (u % p.n_qtiles);
     const int bg = u / p.n_qtiles;
     const int b = bg / p.Hkv;
     const int g = bg - b * p.Hkv;
     const int z_q = b * p.Hq + g * p.G + hi;
     const int z_kv = bg;
     const int q0 = qt * L::BM;
-    const int n = p.n_kvtiles;
+    // Tiles this unit reads: all of them, or (causal) those holding keys <= its last row.
+    const int n = p.causal ? min(p.n_kvtiles, qt + 1) : p.n_kvtiles;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
@@ -322,7 +324,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             for (int i = 0; i < 128; ++i)
                 s[i] = __uint_as_float(sr[i]);
 
-            const int valid = p.Skv - j * L::BN;
+            // keys of this tile the row sees (>= 1): all < Skv, and (causal) <= the row itself
+            const int valid = (p.causal ? min(p.Skv, q0 + row + 1) : p.Skv) - j * L::BN;
             if (valid < L::BN) {
 #pragma unroll
                 for (int i = 1; i < 128; ++i)
@@ -478,9 +481,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
 // Units 2c and 2c+1 share (batch, KV head) exactly when the units of one
 // (batch, KV head), query tiles x heads per group, are even in number.
+// Causal units of one pair must also share the query tile (same tile count):
+// with the head-in-group index fastest that holds when G is even.
 inline bool use_pair(const KernelParams &p, int grid)
 {
-    return !(p.debug_flags & DEBUG_SINGLE_CTA) && ((p.n_qtiles * p.G) % 2 == 0) && (grid % 2 == 0);
+    if (p.debug_flags & DEBUG_SINGLE_CTA)
+        return false;
+    if (p.causal && (p.G % 2) != 0)
+        return false;
+    return ((p.n_qtiles * p.G) % 2 == 0) && (grid % 2 == 0);
 }
 
 template <int D, bool BF16>

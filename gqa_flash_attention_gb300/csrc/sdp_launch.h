@@ -16,6 +16,7 @@ struct KernelParams {
     float c;  // scale * log2(e): scores in base-2 units
     unsigned long long timeout_ns;
     int debug_flags;
+    int causal;  // row i sees keys 0..i only
 };
 
 // Tensor maps of one launch: Q, K, V, O with 128-row boxes, and K with 64-row

@@ -161,6 +161,7 @@ extern "C" int sdp_fwd_noalloc(const void *q, const void *k, const void *v, void
     p.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.timeout_ns = kTimeoutNs;
     p.debug_flags = 0;
+    p.causal = 0;
 
     const int grid = static_cast<int>(units);
     cudaError_t e;

@@ -34,6 +34,7 @@ class Workload:
     seed: int = 0
     peaky_k: bool = False
     scale: float | None = None  # None means 1/sqrt(D)
+    causal: bool = False        # row i sees keys 0..i
     note: str = field(default="", compare=False)
 
     @property
@@ -49,8 +50,13 @@ class Workload:
         return (self.B, self.Hq, self.Hkv, self.Sq, self.Skv, self.D)
 
     def flops(self) -> int:
-        """Matmul FLOPs: 4 * Sq * Skv * D per query head (two contractions)."""
-        return 4 * self.B * self.Hq * self.Sq * self.Skv * self.D
+        """Matmul FLOPs: 4 * D per (query row, key it sees) per query head (two
+        contractions): 4 * Sq * Skv * D, or, causal, 4 * D * sum_i min(i + 1, Skv)."""
+        if not self.causal:
+            return 4 * self.B * self.Hq * self.Sq * self.Skv * self.D
+        full = min(self.Sq, self.Skv)  # rows 0..full-1 see i + 1 keys, the rest see all Skv
+        seen = full * (full + 1) // 2 + (self.Sq - full) * self.Skv
+        return 4 * self.B * self.Hq * seen * self.D
 
     def hbm_bytes(self) -> int:
         """Algorithmic HBM bytes: Q, K, V read once, O written once (16-bit), LSE fp32."""
@@ -78,6 +84,16 @@ WORKLOADS = {
 
 # The pages' headline shape: 32 query heads over 2 KV heads, head dim 256, 16K x 16K.
 HEADLINE = "gqa16_s16k_d256_fp16"
+
+# Causal counterparts (row i sees keys 0..i), the next step of the study; they
+# are benchmark and parity cases beside the five workloads above.
+CAUSAL_WORKLOADS = {
+    "gqa16_s16k_d256_fp16_causal": WORKLOADS["gqa16_s16k_d256_fp16"].with_(name="gqa16_s16k_d256_fp16_causal",
+                                                                           causal=True),
+    "mha_b4_s16k_d128_fp16_causal": WORKLOADS["mha_b4_s16k_d128_fp16"].with_(name="mha_b4_s16k_d128_fp16_causal",
+                                                                             causal=True),
+}
+ALL_WORKLOADS = {**WORKLOADS, **CAUSAL_WORKLOADS}
 
 
 def _normal(rng: np.random.Generator, n: int) -> np.ndarray:

@@ -67,6 +67,18 @@ int sdp_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
             void *stream);
 
 /*
+ * sdp_fwd_causal — sdp_fwd with causal masking: query row i attends to keys
+ * 0..i only (top-left alignment, as PyTorch's is_causal; rows i >= Skv see
+ * every key). The "SyclKittens" summary reports causal attention (sections
+ * E.4, E.6) without fixing a convention. Same arguments, layout, ownership
+ * and errors as sdp_fwd. Key tiles past a query tile's last row are skipped,
+ * so the work is about half of sdp_fwd's when Sq = Skv.
+ */
+int sdp_fwd_causal(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale, int dtype,
+                   void *stream);
+
+/*
  * sdp_fwd_noalloc — sdp_fwd for callers that cannot allocate device memory.
  * The paper has no counterpart: this is a library-usage variant, not a step of
  * the method.
@@ -128,8 +140,9 @@ unsigned int sdp_set_wait_timeout_ms(unsigned int ms);
 /*
  * sdp_set_debug_flags — test hooks, 0 by default. Bit 0: the load warp issues
  * no copies at all, so every consumer wait runs out and the kernel returns
- * through its timeout path (used to test that path without a fault).
- * Returns the previous flags.
+ * through its timeout path (used to test that path without a fault). Bit 1:
+ * always run the single-CTA kernel, never the CTA-pair kernel (both compute
+ * the same result; tests compare them). Returns the previous flags.
  */
 int sdp_set_debug_flags(int flags);
 
@@ -139,7 +152,7 @@ int sdp_last_cuda_error(void);
 /* A static, human-readable description of a status code. */
 const char *sdp_strerror(int code);
 
-/* ABI version: 100 * major + minor. */
+/* ABI version: 100 * major + minor (101: adds sdp_fwd_causal). */
 int sdp_version(void);
 
 /* Free the per-device status words. Call only with no sdp work in flight. */

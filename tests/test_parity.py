@@ -29,7 +29,7 @@ def _built():
     sdp.lib()
 
 
-def gpu_run(q, k, v, scale, guard=4096):
+def gpu_run(q, k, v, scale, guard=4096, causal=False):
     """Run through the C ABI into canary-filled buffers with guard tails."""
     dev = torch.device("cuda")
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -38,7 +38,7 @@ def gpu_run(q, k, v, scale, guard=4096):
     l_buf = torch.full((B * Hq * Sq + guard,), float("nan"), dtype=torch.float32, device=dev)
     o = o_buf[:q.numel()].view(q.shape)
     lse = l_buf[:B * Hq * Sq].view(B, Hq, Sq)
-    sdp.sdp_fwd(qd, kd, vd, scale=scale, out=o, lse=lse)
+    sdp.sdp_fwd(qd, kd, vd, scale=scale, out=o, lse=lse, causal=causal)
     assert sdp.poll_status() == sdp.SDP_OK
     assert torch.isnan(o_buf[q.numel():]).all(), "write past the end of O"
     assert torch.isnan(l_buf[B * Hq * Sq:]).all(), "write past the end of LSE"
@@ -47,8 +47,8 @@ def gpu_run(q, k, v, scale, guard=4096):
 
 def check_full(w: Workload):
     q, k, v = workloads.make_inputs(w)
-    o, lse = gpu_run(q, k, v, w.softmax_scale)
-    ref_o, ref_l = oracle.sdp_fwd(q, k, v, ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale)
+    o, lse = gpu_run(q, k, v, w.softmax_scale, causal=w.causal)
+    ref_o, ref_l = oracle.sdp_fwd(q, k, v, ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale, causal=w.causal)
     st = compare(o, lse, ref_o, ref_l, w.dtype)
     assert_within(st, w.dtype)
     return st
@@ -100,14 +100,14 @@ def test_peaky_keys_small():
     check_full(Workload("peaky", 1, 8, 2, 256, 1024, 128, "bf16", seed=42, peaky_k=True))
 
 
-@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if n != "gqa4_s256_d128_fp16"])
+@pytest.mark.parametrize("name", [n for n in workloads.ALL_WORKLOADS if n != "gqa4_s256_d128_fp16"])
 def test_full_size_workload_sampled_rows(name):
-    w = workloads.WORKLOADS[name]
+    w = workloads.ALL_WORKLOADS[name]
     q, k, v = workloads.make_inputs(w)
-    o, lse = gpu_run(q, k, v, w.softmax_scale)
+    o, lse = gpu_run(q, k, v, w.softmax_scale, causal=w.causal)
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
     rows = workloads.sample_rows(w, 256)
-    ref_o, ref_l = oracle.sdp_fwd_rows(q, k, v, ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale, rows)
+    ref_o, ref_l = oracle.sdp_fwd_rows(q, k, v, ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale, rows, causal=w.causal)
     idx = torch.from_numpy(rows.astype(np.int64)).to(o.device)
     o_s = torch.gather(o, 2, idx[..., None].expand(-1, -1, -1, w.D))
     l_s = torch.gather(lse, 2, idx)
@@ -144,3 +144,32 @@ def test_default_scale_is_inverse_sqrt_d():
     o1, _ = sdp.sdp_fwd(q, k, v)
     o2, _ = sdp.sdp_fwd(q, k, v, scale=1.0 / math.sqrt(256))
     assert torch.equal(o1, o2)
+
+
+# ------------------------------------------------------------------- causal
+
+CAUSAL = []
+for D in (128, 256):
+    for dt in ("fp16", "bf16"):
+        CAUSAL += [
+            Workload(f"causal_sq_eq_skv_gqa2_{D}_{dt}", 1, 4, 2, 300, 300, D, dt, seed=71, causal=True),
+            Workload(f"causal_mha_{D}_{dt}", 2, 2, 2, 257, 257, D, dt, seed=72, causal=True),
+            Workload(f"causal_sq_lt_skv_{D}_{dt}", 1, 4, 1, 129, 400, D, dt, seed=73, causal=True),
+            Workload(f"causal_sq_gt_skv_{D}_{dt}", 1, 2, 1, 300, 130, D, dt, seed=74, causal=True),
+            Workload(f"causal_one_key_{D}_{dt}", 1, 2, 1, 5, 1, D, dt, seed=75, causal=True),
+        ]
+
+
+@pytest.mark.parametrize("w", CAUSAL, ids=lambda w: w.name)
+def test_causal_every_row(w):
+    check_full(w)
+
+
+@pytest.mark.parametrize("w", [w for w in CAUSAL if w.D == 256 and w.dtype == "bf16"], ids=lambda w: w.name)
+def test_causal_single_cta_kernel_every_row(w):
+    old = sdp.set_debug_flags(DEBUG_SINGLE_CTA)
+    try:
+        check_full(w)
+    finally:
+        sdp.set_debug_flags(old)
+

@@ -66,3 +66,11 @@ def test_flop_and_byte_counts():
     w = workloads.WORKLOADS["gqa16_s16k_d256_fp16"]
     assert w.flops() == 4 * 32 * 16384 * 16384 * 256
     assert w.hbm_bytes() == 2 * (2 * 32 * 16384 * 256) + 2 * (2 * 2 * 16384 * 256) + 32 * 16384 * 4
+
+
+def test_causal_flop_count():
+    """Row i sees min(i + 1, Skv) keys; 4 * D FLOPs per (row, key)."""
+    w = Workload("c", 1, 1, 1, 5, 3, 128, causal=True)
+    assert w.flops() == 4 * 128 * (1 + 2 + 3 + 3 + 3)
+    w2 = Workload("c2", 2, 4, 2, 300, 300, 64, causal=True)
+    assert w2.flops() == 4 * 64 * 2 * 4 * (300 * 301 // 2)
