@@ -58,6 +58,8 @@ def _load():
         lib.oracle_fp16_to_double.restype = ctypes.c_double
         lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_sdp_merge.argtypes = [p, p, i, ctypes.c_long, i, p, p]
+        lib.oracle_sdp_merge.restype = i
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i
         _lib = lib
@@ -134,3 +136,24 @@ def row_probs(q, k, v, dtype: int, shape, scale: float, b: int, h: int, i: int, 
     if rc != 0:
         raise ValueError("oracle rejected the shape or row index")
     return p, o, float(lse[0])
+
+
+def sdp_merge(o_parts, lse_parts):
+    """Merge partial results over disjoint key sets (fp64).
+
+    o_parts: [P, rows, D] (any real dtype: numpy, or a torch tensor, upcast
+    exactly to float64); lse_parts: [P, rows]. Returns (o [rows, D], lse [rows]).
+    """
+    def f64(x):
+        if hasattr(x, "detach"):
+            x = x.detach().cpu().double().numpy()
+        return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    op, lp = f64(o_parts), f64(lse_parts)
+    P, rows, D = op.shape
+    assert lp.shape == (P, rows)
+    o = np.empty((rows, D), dtype=np.float64)
+    lse = np.empty(rows, dtype=np.float64)
+    rc = _load().oracle_sdp_merge(_ptr(op), _ptr(lp), int(P), int(rows), int(D), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle rejected the merge sizes")
+    return o, lse

@@ -260,6 +260,49 @@ int oracle_sdp_row_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v
     return status;
 }
 
+/*
+ * Merge of partial attention results over disjoint key sets — the state
+ * exchange of ring / context-parallel attention ("SyclKittens" summary,
+ * section I.2: each step merges the online-softmax state of the next key
+ * shard). For each row r, with parts p = 0..P-1 each holding a normalised
+ * output O_p[r,:] over its keys and the log-sum-exp LSE_p[r] of its scores:
+ *
+ *   LSE[r] = ln sum_p exp(LSE_p[r])          (taken relative to M = max_p LSE_p)
+ *   O[r,:] = sum_p exp(LSE_p[r] - LSE[r]) * O_p[r,:]
+ *
+ * which is attention over the union of the parts' keys. A part with
+ * LSE_p = -inf (no keys) gets weight 0; at least one part must be finite.
+ * o_parts double [P, rows, D], lse_parts double [P, rows]; o_out double
+ * [rows, D], lse_out double [rows]. Returns 0, or -1 on bad sizes.
+ */
+int oracle_sdp_merge(const double *o_parts, const double *lse_parts, int P, long rows, int D,
+                     double *o_out, double *lse_out)
+{
+    if (P <= 0 || rows < 0 || D <= 0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r) {
+        double M = -INFINITY;
+        for (int p = 0; p < P; ++p)
+            if (lse_parts[(size_t)p * rows + r] > M)
+                M = lse_parts[(size_t)p * rows + r];
+        double sum = 0.0;
+        for (int p = 0; p < P; ++p)
+            sum += exp(lse_parts[(size_t)p * rows + r] - M);
+        const double lse = M + log(sum);
+        for (int d = 0; d < D; ++d)
+            o_out[(size_t)r * D + d] = 0.0;
+        for (int p = 0; p < P; ++p) {
+            const double w = exp(lse_parts[(size_t)p * rows + r] - lse);
+            const double *op = o_parts + ((size_t)p * rows + r) * D;
+            for (int d = 0; d < D; ++d)
+                o_out[(size_t)r * D + d] += w * op[d];
+        }
+        lse_out[r] = lse;
+    }
+    return 0;
+}
+
 /* Threads an OpenMP parallel region of the oracle uses (1 without OpenMP). */
 int oracle_num_threads(void)
 {

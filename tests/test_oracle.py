@@ -320,3 +320,47 @@ def test_causal_weights_vanish_past_the_diagonal():
         p, _, _ = oracle.row_probs(q, k, v, FP16, shape, 0.4, 0, 1, i, causal=True)
         assert (p[i + 1:] == 0).all() and (p[:i + 1] > 0).all()
         assert abs(p.sum() - 1.0) <= 1e-12
+
+
+# -------------------------------------------------------------------- merge
+
+@pytest.mark.parametrize("splits", [[7], [3, 4], [1, 5, 9, 2], [10, 0, 7]])
+def test_merge_of_key_splits_equals_full_attention(splits):
+    """Attention over disjoint key sets, merged through the log-sum-exps, is
+    attention over their union (empty sets enter with LSE = -inf)."""
+    Skv = sum(splits)
+    shape = (1, 4, 2, 6, Skv, 16)
+    q, k, v = rand_qkv(*shape, FP16, seed=81 + Skv)
+    full_o, full_l = oracle.sdp_fwd(q, k, v, FP16, shape, 0.4)
+    parts_o, parts_l, start = [], [], 0
+    for n in splits:
+        if n == 0:
+            parts_o.append(np.zeros_like(full_o))
+            parts_l.append(np.full(full_l.shape, -np.inf))
+            continue
+        ks, vs = k[:, :, start:start + n].contiguous(), v[:, :, start:start + n].contiguous()
+        o_s, l_s = oracle.sdp_fwd(q, ks, vs, FP16, (1, 4, 2, 6, n, 16), 0.4)
+        parts_o.append(o_s)
+        parts_l.append(l_s)
+        start += n
+    P = len(splits)
+    o, lse = oracle.sdp_merge(np.stack(parts_o).reshape(P, -1, 16), np.stack(parts_l).reshape(P, -1))
+    assert np.abs(o - full_o.reshape(-1, 16)).max() <= 1e-12
+    assert np.abs(lse - full_l.reshape(-1)).max() <= 1e-12
+
+
+def test_merge_closed_forms():
+    rng = np.random.default_rng(5)
+    o1 = rng.standard_normal((1, 9, 8))
+    l1 = rng.standard_normal((1, 9))
+    o, lse = oracle.sdp_merge(o1, l1)  # one part: identity
+    assert np.array_equal(o, o1[0]) and np.abs(lse - l1[0]).max() <= 1e-15
+    parts = rng.standard_normal((4, 9, 8))
+    same = np.broadcast_to(l1, (4, 9)).copy()
+    o, lse = oracle.sdp_merge(parts, same)  # equal weights: the mean, LSE + ln 4
+    assert np.abs(o - parts.mean(axis=0)).max() <= 1e-14
+    assert np.abs(lse - (l1[0] + math.log(4))).max() <= 1e-14
+    two_l = np.stack([np.zeros(9), np.full(9, math.log(3.0))])  # weights 1/4 and 3/4
+    o, lse = oracle.sdp_merge(parts[:2], two_l)
+    assert np.abs(o - (0.25 * parts[0] + 0.75 * parts[1])).max() <= 1e-14
+    assert np.abs(lse - math.log(4.0)).max() <= 1e-14
