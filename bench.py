@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--cpu-rows", type=int, default=0, help="query rows per head in the CPU sample (0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["attention", "merge"], default="attention",
+                    help="merge: time sdp_merge (HBM-bound) on a context-parallel-shaped case instead")
+    ap.add_argument("--merge-parts", type=int, default=8)
     return ap.parse_args()
 
 
@@ -347,10 +350,55 @@ def ours_arm(args, w):
         torch.distributed.destroy_process_group()
 
 
+def merge_arm(args, w):
+    """sdp_merge of P partial results per row (one per key shard, as in ring
+    attention) for every (batch, head, query row) of the workload."""
+    import gqa_flash_attention_gb300 as sdp
+    dev = torch.device("cuda", 0)
+    P, rows = args.merge_parts, w.B * w.Hq * w.Sq
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    o_parts = torch.randn(P, rows, w.D, device=dev, generator=g).to(w.torch_dtype)
+    lse_parts = torch.randn(P, rows, device=dev, generator=g) * 3
+    o = torch.empty(rows, w.D, dtype=w.torch_dtype, device=dev)
+    lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        sdp.sdp_merge(o_parts, lse_parts, out=o, lse=lse)
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    clocks = ClockSampler(0)
+    clocks.start()
+    torch.cuda.synchronize(dev)
+    ev[0].record()
+    for i in range(K):
+        sdp.sdp_merge(o_parts, lse_parts, out=o, lse=lse)
+        ev[i + 1].record()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(K))
+    nbytes = P * rows * (w.D * 2 + 4) + rows * (w.D * 2 + 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak = 6677.5
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            peak = float(json.load(f)["hbm_gbs"])
+    print(json.dumps({
+        "metric": "sdp_merge HBM GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"merge of {P} parts over {w.name} rows", "parts": P, "rows": rows, "D": w.D,
+                   "l2": "inputs larger than L2; no flush"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": None, "kernel": "merge_kernel", "bytes_per_launch": nbytes},
+        "clocks": clk, "gpu_launches": K}), flush=True)
+
+
 def main():
     args = parse()
     w = workloads.ALL_WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.op == "merge":
+        merge_arm(args, w)
+    elif args.impl == "reference":
         reference_arm(args, w)
     else:
         ours_arm(args, w)

@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.sdp_fwd.restype = i
         L.sdp_fwd_causal.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         L.sdp_fwd_causal.restype = i
+        L.sdp_merge.argtypes = [vp, vp, i, ctypes.c_longlong, i, i, vp, vp, vp]
+        L.sdp_merge.restype = i
         L.sdp_poll_status.argtypes = [vp]
         L.sdp_poll_status.restype = i
         L.sdp_last_status_detail.argtypes = []
@@ -142,6 +144,37 @@ def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
         rc = sdp_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                          0 if lse is None else lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
                          _DTYPE_CODE[q.dtype], _stream_handle(stream, q.device), causal=causal)
+    _check(rc)
+    return out, lse
+
+
+def sdp_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor | None = None,
+              lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
+    """Merge partial attention results over disjoint key sets.
+
+    o_parts: [P, ...rows..., D] fp16/bf16 (each part's normalised output, e.g.
+    sdp_fwd over one key shard), lse_parts: [P, ...rows...] fp32. Returns
+    (o [...rows..., D], lse [...rows...]) over the union of the keys.
+    """
+    if not (o_parts.is_cuda and lse_parts.is_cuda) or o_parts.device != lse_parts.device:
+        raise ValueError("o_parts and lse_parts must be CUDA tensors on one device")
+    if o_parts.dtype not in _DTYPE_CODE or lse_parts.dtype != torch.float32:
+        raise ValueError("o_parts must be float16/bfloat16 and lse_parts float32")
+    if not (o_parts.is_contiguous() and lse_parts.is_contiguous()):
+        raise ValueError("o_parts and lse_parts must be contiguous")
+    P, D = o_parts.shape[0], o_parts.shape[-1]
+    if tuple(lse_parts.shape) != tuple(o_parts.shape[:-1]):
+        raise ValueError("lse_parts must be o_parts' shape without the last dimension")
+    rows = lse_parts.numel() // P
+    if out is None:
+        out = torch.empty(o_parts.shape[1:], dtype=o_parts.dtype, device=o_parts.device)
+    if lse is None and return_lse:
+        lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    with torch.cuda.device(o_parts.device):
+        rc = int(lib().sdp_merge(ctypes.c_void_p(o_parts.data_ptr()), ctypes.c_void_p(lse_parts.data_ptr()), int(P),
+                                 int(rows), int(D), _DTYPE_CODE[o_parts.dtype], ctypes.c_void_p(out.data_ptr()),
+                                 ctypes.c_void_p(0 if lse is None else lse.data_ptr()),
+                                 ctypes.c_void_p(_stream_handle(stream, o_parts.device))))
     _check(rc)
     return out, lse
 

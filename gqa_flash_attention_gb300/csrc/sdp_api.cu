@@ -256,7 +256,7 @@ const char *sdp_strerror(int code)
     }
 }
 
-int sdp_version(void) { return 101; }
+int sdp_version(void) { return 102; }
 
 void sdp_shutdown(void)
 {

@@ -79,6 +79,27 @@ int sdp_fwd_causal(const void *q, const void *k, const void *v, void *o, float *
                    void *stream);
 
 /*
+ * sdp_merge — combine partial results over disjoint key sets into the result
+ * over their union: the state exchange of ring / context-parallel attention
+ * ("SyclKittens" summary, section I.2). For every row r:
+ *
+ *     LSE[r] = ln sum_p exp(LSE_p[r]),    O[r,:] = sum_p exp(LSE_p[r] - LSE[r]) * O_p[r,:]
+ *
+ * o_parts   device, [nparts, rows, D] contiguous, dtype elements: each part's
+ *           normalised output (e.g. sdp_fwd's o over one key shard)
+ * lse_parts device, [nparts, rows] fp32: each part's log-sum-exp (sdp_fwd's
+ *           lse); -inf marks a part without keys; at least one part per row
+ *           must be finite
+ * o         device, [rows, D] dtype (written); lse [rows] fp32 (written) or NULL
+ * rows = B*H*Sq for sdp_fwd's layouts; D in {128, 256}; dtype SDP_FP16/BF16.
+ * Weights and sums in fp32, output rounded to nearest even. Buffers 16-byte
+ * aligned (lse 4-byte); o must not alias o_parts. Enqueued on `stream`;
+ * validation errors launch nothing; a failed launch returns SDP_ERR_CUDA.
+ */
+int sdp_merge(const void *o_parts, const float *lse_parts, int nparts, long long rows, int D, int dtype,
+              void *o, float *lse, void *stream);
+
+/*
  * sdp_fwd_noalloc — sdp_fwd for callers that cannot allocate device memory.
  * The paper has no counterpart: this is a library-usage variant, not a step of
  * the method.
@@ -152,7 +173,7 @@ int sdp_last_cuda_error(void);
 /* A static, human-readable description of a status code. */
 const char *sdp_strerror(int code);
 
-/* ABI version: 100 * major + minor (101: adds sdp_fwd_causal). */
+/* ABI version: 100 * major + minor (101: sdp_fwd_causal; 102: sdp_merge). */
 int sdp_version(void);
 
 /* Free the per-device status words. Call only with no sdp work in flight. */
