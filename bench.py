@@ -72,6 +72,14 @@ def load_peaks():
     return FALLBACK_PEAK_TFLOPS, 1700.0, "fallback"
 
 
+def load_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
 def source_hash():
     import hashlib
     h = hashlib.sha256()
@@ -214,20 +222,39 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+def launch_shape(w):
+    """(Sq, G) of the launch: without a causal mask the G query heads of a KV
+    group run as one head of G * Sq rows when Sq is not a multiple of 128."""
+    G = w.Hq // w.Hkv
+    if not w.causal and G > 1 and w.Sq % 128:
+        return w.Sq * G, 1
+    return w.Sq, G
+
+
 def kernel_name(w):
     """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
     the units of each (batch, KV head) pair up (and, causal, share the query
-    tile), else the single-CTA kernel."""
-    n_qtiles = (w.Sq + 127) // 128
-    G = w.Hq // w.Hkv
+    tile), else the single-CTA kernel; split-KV adds the merge kernel."""
+    sq, G = launch_shape(w)
+    n_qtiles = (sq + 127) // 128
     pair = (n_qtiles * G) % 2 == 0 and not (w.causal and G % 2)
-    return "sdp_fwd_pair_kernel" if pair else "sdp_fwd_kernel"
+    name = "sdp_fwd_pair_kernel" if pair else "sdp_fwd_kernel"
+    return name + " + merge_kernel" if w.kv_splits != 1 else name
+
+
+L2_BYTES = 126 * 2 ** 20
+
+
+def needs_flush(w):
+    return w.hbm_bytes() < 2 * L2_BYTES
 
 
 def config_of(w, n):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv, "D": w.D,
             "io_dtype": w.dtype, "scale": w.softmax_scale, "causal": w.causal, "peaky_k": w.peaky_k,
-            "flops_per_step_per_gpu": w.flops(), "l2": "inputs larger than L2 (Q and O exceed 126 MB); no flush",
+            "flops_per_step_per_gpu": w.flops(), "kv_splits": w.kv_splits,
+            "l2": ("L2 flushed (256 MB write) before every timed step; only the call is timed" if needs_flush(w)
+                   else "inputs larger than L2; no flush"),
             "parallelism": "replicas" if n > 1 else "single GPU"}
 
 
@@ -248,29 +275,47 @@ def ours_arm(args, w):
     lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    launches_per_step = 1
+    ws = None
+    if w.kv_splits != 1:
+        dt = sdp.SDP_BF16 if w.dtype == "bf16" else sdp.SDP_FP16
+        splits = sdp.splitkv_count(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, dt, w.kv_splits)
+        need = sdp.splitkv_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, dt, w.kv_splits)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        launches_per_step = 2 if splits > 1 else 1
+
+    def call():
+        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse, causal=w.causal, kv_splits=w.kv_splits,
+                    workspace=ws)
+
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev) if needs_flush(w) else None
     for _ in range(args.warmup):
-        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse, causal=w.causal)
+        call()
     torch.cuda.synchronize(dev)
     if sdp.poll_status() != sdp.SDP_OK:
         raise RuntimeError("kernel reported a timeout during warm-up")
 
     K = args.steps
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     clocks = ClockSampler(dev.index)
     clocks.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    ev[0].record(stream)
     for i in range(K):
-        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse, causal=w.causal)
-        ev[i + 1].record(stream)
+        if flush is not None:
+            flush.zero_()
+        ev0[i].record(stream)
+        call()
+        ev1[i].record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
-    total_ms = ev[0].elapsed_time(ev[K])
+    per_launch_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
+    # back to back, the whole region is the time; with flushes between steps, the sum of the steps
+    total_ms = sum(per_launch_ms) if flush is not None else ev0[0].elapsed_time(ev1[K - 1])
     if sdp.poll_status() != sdp.SDP_OK:
         raise RuntimeError("kernel reported a timeout in the timed region")
 
@@ -293,7 +338,7 @@ def ours_arm(args, w):
             q.copy_(qp, non_blocking=True)
             k.copy_(kp, non_blocking=True)
             v.copy_(vp, non_blocking=True)
-            sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse, causal=w.causal)
+            call()
             op.copy_(o, non_blocking=True)
             lp.copy_(lse, non_blocking=True)
 
@@ -322,13 +367,23 @@ def ours_arm(args, w):
         return
 
     peak, peak_sus, peak_src = load_peaks()
+    hbm_peak, hbm_src = load_hbm_peak()
     avg_launch_ms = statistics.mean(per_launch_ms)
-    achieved = w.flops() / (avg_launch_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": load_traffic(w.name),
-                "peak_source": f"{peak_src} bf16 dense (burst); fp16 runs at the same tensor rate",
-                "frac_of_sustained": achieved / peak_sus, "kernel": kernel_name(w),
-                "launch_ms_median": statistics.median(per_launch_ms)}
+    tflops = w.flops() / (avg_launch_ms * 1e-3) / 1e12
+    intensity = w.flops() / w.hbm_bytes()  # FLOP per algorithmic HBM byte
+    if intensity >= peak * 1e12 / (hbm_peak * 1e9):
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                    "frac": tflops / peak, "traffic": load_traffic(w.name),
+                    "peak_source": f"{peak_src} bf16 dense (burst); fp16 runs at the same tensor rate",
+                    "frac_of_sustained": tflops / peak_sus}
+    else:
+        gbs = w.hbm_bytes() / (avg_launch_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                    "traffic": load_traffic(w.name), "peak_source": f"{hbm_src} HBM copy bandwidth",
+                    "algorithmic_bytes": w.hbm_bytes(), "tflops": tflops}
+    roofline.update({"kernel": kernel_name(w), "launch_ms_median": statistics.median(per_launch_ms),
+                     "flop_per_byte": intensity})
+    achieved = tflops
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -343,7 +398,8 @@ def ours_arm(args, w):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic", "config": config_of(w, world),
         "pct_of_peak": 100.0 * achieved / peak,
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": K,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+        "gpu_launches": K * launches_per_step,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -377,11 +433,7 @@ def merge_arm(args, w):
     ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(K))
     nbytes = P * rows * (w.D * 2 + 4) + rows * (w.D * 2 + 4)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    peak = 6677.5
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(path):
-        with open(path) as f:
-            peak = float(json.load(f)["hbm_gbs"])
+    peak, _ = load_hbm_peak()
     print(json.dumps({
         "metric": "sdp_merge HBM GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

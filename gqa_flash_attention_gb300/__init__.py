@@ -57,6 +57,12 @@ def lib() -> ctypes.CDLL:
         L.sdp_fwd_causal.restype = i
         L.sdp_merge.argtypes = [vp, vp, i, ctypes.c_longlong, i, i, vp, vp, vp]
         L.sdp_merge.restype = i
+        L.sdp_fwd_splitkv_count.argtypes = [i, i, i, i, i, i, i, i]
+        L.sdp_fwd_splitkv_count.restype = i
+        L.sdp_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        L.sdp_fwd_splitkv_workspace_bytes.restype = ctypes.c_longlong
+        L.sdp_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, ctypes.c_ulonglong, vp]
+        L.sdp_fwd_splitkv.restype = i
         L.sdp_poll_status.argtypes = [vp]
         L.sdp_poll_status.restype = i
         L.sdp_last_status_detail.argtypes = []
@@ -106,9 +112,35 @@ def sdp_fwd_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: int, Hkv: 
                              ctypes.c_float(scale), int(dtype), ctypes.c_void_p(stream)))
 
 
+def sdp_fwd_splitkv_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: int, Hkv: int, Sq: int, Skv: int,
+                        D: int, scale: float, dtype: int, n_splits: int, workspace: int, workspace_bytes: int,
+                        stream: int = 0) -> int:
+    """The raw C call sdp_fwd_splitkv with integer addresses; returns the status code."""
+    return int(lib().sdp_fwd_splitkv(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v),
+                                     ctypes.c_void_p(o), ctypes.c_void_p(lse), int(B), int(Hq), int(Hkv), int(Sq),
+                                     int(Skv), int(D), ctypes.c_float(scale), int(dtype), int(n_splits),
+                                     ctypes.c_void_p(workspace), ctypes.c_ulonglong(workspace_bytes),
+                                     ctypes.c_void_p(stream)))
+
+
+def splitkv_count(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int, dtype: int, n_splits: int = 0) -> int:
+    """Split count sdp_fwd_splitkv uses for these sizes on the current device (0 = automatic)."""
+    rc = int(lib().sdp_fwd_splitkv_count(B, Hq, Hkv, Sq, Skv, D, dtype, n_splits))
+    _check(min(rc, 0))
+    return rc
+
+
+def splitkv_workspace_bytes(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int, dtype: int,
+                            n_splits: int = 0) -> int:
+    """Workspace bytes sdp_fwd_splitkv needs for these sizes on the current device."""
+    rc = int(lib().sdp_fwd_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Skv, D, dtype, n_splits))
+    _check(min(rc, 0))
+    return rc
+
+
 def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
             out: torch.Tensor | None = None, lse: torch.Tensor | None = None, return_lse: bool = True,
-            stream=None, causal: bool = False):
+            stream=None, causal: bool = False, kv_splits: int = 1, workspace: torch.Tensor | None = None):
     """Grouped-query attention forward on sm_103a (causal: row i sees keys 0..i).
 
     q: [B, Hq, Sq, D]; k, v: [B, Hkv, Skv, D]; fp16 or bf16, contiguous, on one
@@ -116,6 +148,11 @@ def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
     like q and lse fp32 [B, Hq, Sq] (None when return_lse is False and no lse
     buffer is given). The work is enqueued on `stream` (default: the current
     stream) and not synchronised.
+
+    kv_splits != 1 (0 = automatic) runs the split-KV forward for problems with
+    few query tiles (decode): the keys are cut into runs whose partial results
+    are merged. Its scratch is `workspace` (a contiguous CUDA byte tensor) or,
+    when None, a tensor from torch's allocator. Not combinable with causal.
     """
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D [B, H, S, D]")
@@ -140,6 +177,25 @@ def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
     if lse is not None and (lse.shape != (B, Hq, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous()
                             or lse.device != q.device):
         raise ValueError("lse must be a contiguous float32 tensor [B, Hq, Sq] on q's device")
+    if kv_splits != 1:
+        if causal:
+            raise ValueError("the split-KV forward has no causal mask")
+        with torch.cuda.device(q.device):
+            dt = _DTYPE_CODE[q.dtype]
+            need = splitkv_workspace_bytes(B, Hq, Hkv, Sq, Skv, D, dt, kv_splits)
+            if workspace is None:
+                workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+                if isinstance(stream, torch.cuda.Stream):
+                    workspace.record_stream(stream)
+            elif not (workspace.is_cuda and workspace.device == q.device and workspace.is_contiguous()):
+                raise ValueError("workspace must be a contiguous tensor on q's device")
+            rc = sdp_fwd_splitkv_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     0 if lse is None else lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
+                                     dt, kv_splits, workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream_handle(stream, q.device))
+        _check(rc)
+        return out, lse
     with torch.cuda.device(q.device):
         rc = sdp_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                          0 if lse is None else lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <initializer_list>
 #include <mutex>
 
 #include "sdp.h"
@@ -110,10 +111,11 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 namespace {
 
-int forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
-            int Skv, int D, float scale, int dtype, int causal, void *stream)
+constexpr int kDebugNoPack = 4;  // host-side test hook: never pack the query heads of a group
+
+int validate(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int Hq, int Hkv,
+             int Sq, int Skv, int D, float scale, int dtype)
 {
-    // ---- validation: no CUDA call happens before all of it passes
     if (dtype != SDP_FP16 && dtype != SDP_BF16)
         return SDP_ERR_UNSUPPORTED;
     if (D != 128 && D != 256)
@@ -128,56 +130,158 @@ int forward(const void *q, const void *k, const void *v, void *o, float *lse, in
         return SDP_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
         return SDP_ERR_ALIGNMENT;
-    const long long n_qtiles = (static_cast<long long>(Sq) + 127) / 128;
-    const long long n_kvtiles = (static_cast<long long>(Skv) + 127) / 128;
-    const long long planes_q = static_cast<long long>(B) * Hq;
-    const long long planes_kv = static_cast<long long>(B) * Hkv;
-    const long long units = planes_q * n_qtiles;
-    if (planes_q > INT32_MAX || planes_kv > INT32_MAX || units > INT32_MAX)
+    return SDP_OK;
+}
+
+// The launch shape of one call. Without causal masking, the G query heads of
+// a KV group are packed into one head of G * Sq rows when Sq is not a
+// multiple of the 128-row query tile: Q[b, g*G + hi, i] sits at row
+// hi * Sq + i of plane (b, g) of the same buffer, so this is only a different
+// view (O and LSE likewise), and every packed row still reads KV plane (b, g).
+// It fills the tiles that small Sq (decode: Sq = 1) leaves mostly empty.
+struct Shape {
+    int Hq, G, Sq;  // after packing
+    long long n_qtiles, n_kvtiles, planes_q, planes_kv, units;
+    int splits, tiles_per_split;
+};
+
+int shape_of(int B, int Hq, int Hkv, int Sq, int Skv, int causal, Shape *sh)
+{
+    const int G = Hq / Hkv;
+    const bool pack = !causal && G > 1 && Sq % 128 != 0 && static_cast<long long>(G) * Sq <= INT32_MAX &&
+                      !(g_debug_flags.load() & kDebugNoPack);
+    sh->Hq = pack ? Hkv : Hq;
+    sh->G = pack ? 1 : G;
+    sh->Sq = pack ? G * Sq : Sq;
+    sh->n_qtiles = (static_cast<long long>(sh->Sq) + 127) / 128;
+    sh->n_kvtiles = (static_cast<long long>(Skv) + 127) / 128;
+    sh->planes_q = static_cast<long long>(B) * sh->Hq;
+    sh->planes_kv = static_cast<long long>(B) * Hkv;
+    sh->units = sh->planes_q * sh->n_qtiles;
+    sh->splits = 1;
+    sh->tiles_per_split = static_cast<int>(sh->n_kvtiles > INT32_MAX ? INT32_MAX : sh->n_kvtiles);
+    if (sh->planes_q > INT32_MAX || sh->planes_kv > INT32_MAX || sh->units > INT32_MAX)
         return SDP_ERR_OVERFLOW;
+    return SDP_OK;
+}
 
-    // ---- device
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return cuda_fail(e);
-    unsigned int *status = nullptr;
-    int rc = device_state(dev, &status);
-    if (rc != SDP_OK)
-        return rc;
+// Split count for a split-KV call: `requested` (0 = enough units to cover the
+// SMs once), clamped to [1, KV tiles], then evened out so that every split
+// reads the same number of tiles except a shorter last one.
+int set_splits(Shape *sh, int requested, int sms)
+{
+    long long s = requested;
+    if (s <= 0)
+        s = sh->units >= sms ? 1 : (sms + sh->units - 1) / sh->units;
+    s = s < 1 ? 1 : (s > sh->n_kvtiles ? sh->n_kvtiles : s);
+    const long long tps = (sh->n_kvtiles + s - 1) / s;
+    s = (sh->n_kvtiles + tps - 1) / tps;
+    if (s * sh->planes_q > INT32_MAX || s * sh->units > INT32_MAX)
+        return SDP_ERR_OVERFLOW;
+    sh->splits = static_cast<int>(s);
+    sh->tiles_per_split = static_cast<int>(tps);
+    return SDP_OK;
+}
 
+long long align256(long long x) { return (x + 255) & ~255LL; }
+
+// Workspace of a split-KV call: partial O [splits, B*Hq*Sq, D] (I/O dtype),
+// then partial LSE [splits, B*Hq*Sq] fp32 at the next 256-byte boundary.
+long long workspace_bytes(const Shape &sh, int D)
+{
+    if (sh.splits <= 1)
+        return 0;
+    const long long rows = sh.planes_q * sh.Sq;
+    return align256(sh.splits * rows * D * 2) + sh.splits * rows * 4;
+}
+
+int sm_count(int dev, int *sms)
+{
+    cudaError_t e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    return e == cudaSuccess ? SDP_OK : cuda_fail(e);
+}
+
+// Encode the maps and launch the kernel for `sh`. O / LSE go to `o` / `lse`
+// ([splits * planes_q, Sq, D] and [splits * planes_q, Sq] when splits > 1).
+int launch(const Shape &sh, const void *q, const void *k, const void *v, void *o, float *lse, int Hkv, int Skv,
+           int D, float scale, int dtype, int causal, unsigned int *status, cudaStream_t st)
+{
     sdp::LaunchMaps maps;
-    if ((rc = encode_map(&maps.q, q, dtype, D, Sq, planes_q)) != SDP_OK ||
-        (rc = encode_map(&maps.k, k, dtype, D, Skv, planes_kv)) != SDP_OK ||
-        (rc = encode_map(&maps.k_half, k, dtype, D, Skv, planes_kv, 64)) != SDP_OK ||
-        (rc = encode_map(&maps.v, v, dtype, D, Skv, planes_kv)) != SDP_OK ||
-        (rc = encode_map(&maps.o, o, dtype, D, Sq, planes_q)) != SDP_OK)
+    int rc;
+    const long long out_planes = sh.planes_q * sh.splits;
+    if ((rc = encode_map(&maps.q, q, dtype, D, sh.Sq, sh.planes_q)) != SDP_OK ||
+        (rc = encode_map(&maps.k, k, dtype, D, Skv, sh.planes_kv)) != SDP_OK ||
+        (rc = encode_map(&maps.k_half, k, dtype, D, Skv, sh.planes_kv, 64)) != SDP_OK ||
+        (rc = encode_map(&maps.v, v, dtype, D, Skv, sh.planes_kv)) != SDP_OK ||
+        (rc = encode_map(&maps.o, o, dtype, D, sh.Sq, out_planes)) != SDP_OK)
         return rc;
 
     sdp::KernelParams p{};
     p.lse = lse;
     p.status = status;
-    p.Hq = Hq;
+    p.Hq = sh.Hq;
     p.Hkv = Hkv;
-    p.G = Hq / Hkv;
-    p.Sq = Sq;
+    p.G = sh.G;
+    p.Sq = sh.Sq;
     p.Skv = Skv;
-    p.n_qtiles = static_cast<int>(n_qtiles);
-    p.n_kvtiles = static_cast<int>(n_kvtiles);
+    p.n_qtiles = static_cast<int>(sh.n_qtiles);
+    p.n_kvtiles = static_cast<int>(sh.n_kvtiles);
     p.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);  // scale * log2(e)
     p.timeout_ns = static_cast<unsigned long long>(g_timeout_ms.load()) * 1000000ull;
     p.debug_flags = g_debug_flags.load();
     p.causal = causal ? 1 : 0;
+    p.kv_splits = sh.splits;
+    p.tiles_per_split = sh.tiles_per_split;
+    p.planes_q = static_cast<int>(sh.planes_q);
 
-    const int grid = static_cast<int>(units);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int grid = static_cast<int>(sh.units * sh.splits);
+    cudaError_t e;
     if (D == 128)
         e = dtype == SDP_BF16 ? sdp::launch_d128_bf16(maps, p, grid, st) : sdp::launch_d128_fp16(maps, p, grid, st);
     else
         e = dtype == SDP_BF16 ? sdp::launch_d256_bf16(maps, p, grid, st) : sdp::launch_d256_fp16(maps, p, grid, st);
+    return e == cudaSuccess ? SDP_OK : cuda_fail(e);
+}
+
+int forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
+            int Skv, int D, float scale, int dtype, int causal, void *stream)
+{
+    // validation: no CUDA call happens before all of it passes
+    int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, dtype);
+    if (rc != SDP_OK)
+        return rc;
+    Shape sh;
+    if ((rc = shape_of(B, Hq, Hkv, Sq, Skv, causal, &sh)) != SDP_OK)
+        return rc;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return cuda_fail(e);
-    return SDP_OK;
+    unsigned int *status = nullptr;
+    if ((rc = device_state(dev, &status)) != SDP_OK)
+        return rc;
+    return launch(sh, q, k, v, o, lse, Hkv, Skv, D, scale, dtype, causal, status, static_cast<cudaStream_t>(stream));
+}
+
+// Shape of a split-KV call on the current device (validation of the sizes only).
+int splitkv_shape(int B, int Hq, int Hkv, int Sq, int Skv, int D, int dtype, int n_splits, Shape *sh, int *dev)
+{
+    if (dtype != SDP_FP16 && dtype != SDP_BF16)
+        return SDP_ERR_UNSUPPORTED;
+    if (D != 128 && D != 256)
+        return SDP_ERR_UNSUPPORTED;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || Hq % Hkv != 0 || n_splits < 0)
+        return SDP_ERR_INVALID_ARG;
+    int rc = shape_of(B, Hq, Hkv, Sq, Skv, 0, sh);
+    if (rc != SDP_OK)
+        return rc;
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    int sms = 0;
+    if ((rc = sm_count(*dev, &sms)) != SDP_OK)
+        return rc;
+    return set_splits(sh, n_splits, sms);
 }
 
 }  // namespace
@@ -194,6 +298,61 @@ int sdp_fwd_causal(const void *q, const void *k, const void *v, void *o, float *
                    int Skv, int D, float scale, int dtype, void *stream)
 {
     return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, dtype, 1, stream);
+}
+
+long long sdp_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int D, int dtype, int n_splits)
+{
+    Shape sh;
+    int dev = 0;
+    const int rc = splitkv_shape(B, Hq, Hkv, Sq, Skv, D, dtype, n_splits, &sh, &dev);
+    return rc != SDP_OK ? rc : workspace_bytes(sh, D);
+}
+
+int sdp_fwd_splitkv_count(int B, int Hq, int Hkv, int Sq, int Skv, int D, int dtype, int n_splits)
+{
+    Shape sh;
+    int dev = 0;
+    const int rc = splitkv_shape(B, Hq, Hkv, Sq, Skv, D, dtype, n_splits, &sh, &dev);
+    return rc != SDP_OK ? rc : sh.splits;
+}
+
+int sdp_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
+                    int Skv, int D, float scale, int dtype, int n_splits, void *workspace,
+                    unsigned long long workspace_bytes_given, void *stream)
+{
+    int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, dtype);
+    if (rc != SDP_OK)
+        return rc;
+    if (n_splits < 0)
+        return SDP_ERR_INVALID_ARG;
+    Shape sh;
+    int dev = 0;
+    if ((rc = splitkv_shape(B, Hq, Hkv, Sq, Skv, D, dtype, n_splits, &sh, &dev)) != SDP_OK)
+        return rc;
+    const long long need = workspace_bytes(sh, D);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes_given < static_cast<unsigned long long>(need))
+            return SDP_ERR_INVALID_ARG;
+        if (!aligned(workspace, 16))
+            return SDP_ERR_ALIGNMENT;
+        const char *w0 = static_cast<const char *>(workspace);
+        const char *w1 = w0 + need;
+        for (const void *x : {q, k, v, static_cast<const void *>(o)})
+            if (static_cast<const char *>(x) >= w0 && static_cast<const char *>(x) < w1)
+                return SDP_ERR_INVALID_ARG;
+    }
+    unsigned int *status = nullptr;
+    if ((rc = device_state(dev, &status)) != SDP_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (sh.splits == 1)
+        return launch(sh, q, k, v, o, lse, Hkv, Skv, D, scale, dtype, 0, status, st);
+    const long long rows = sh.planes_q * sh.Sq;
+    char *ws_o = static_cast<char *>(workspace);
+    float *ws_lse = reinterpret_cast<float *>(ws_o + align256(sh.splits * rows * D * 2));
+    if ((rc = launch(sh, q, k, v, ws_o, ws_lse, Hkv, Skv, D, scale, dtype, 0, status, st)) != SDP_OK)
+        return rc;
+    return sdp_merge(ws_o, ws_lse, sh.splits, rows, D, dtype, o, lse, stream);
 }
 
 int sdp_poll_status(void *stream)
@@ -256,7 +415,7 @@ const char *sdp_strerror(int code)
     }
 }
 
-int sdp_version(void) { return 102; }
+int sdp_version(void) { return 103; }
 
 void sdp_shutdown(void)
 {

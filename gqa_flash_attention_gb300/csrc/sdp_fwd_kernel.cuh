@@ -214,6 +214,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Unit order: head-in-group fastest, then query tile, then (batch, KV head),
     // so CTAs resident together read the same K/V tiles from L2.
     int u = blockIdx.x;
+    // KV split (split-KV launches): the outermost unit coordinate.
+    const int units_per_split = static_cast<int>(gridDim.x) / p.kv_splits;
+    const int split = u / units_per_split;
+    u -= split * units_per_split;
     const int hi = u % p.G;
     u /= p.G;
     // Causal units do qt + 1 tiles: start the longest ones first.
@@ -225,7 +229,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int z_kv = bg;                      // (b, g) plane of K and V
     const int q0 = qt * L::BM;
     // Tiles this unit reads: all of them, or (causal) those holding keys <= its last row.
-    const int n = p.causal ? min(p.n_kvtiles, qt + 1) : p.n_kvtiles;
+    const int t0 = split * p.tiles_per_split;  // first KV tile of this unit
+    const int n = p.causal ? min(p.n_kvtiles, qt + 1) : min(p.n_kvtiles - t0, p.tiles_per_split);
+    const int z_out = split * p.planes_q + z_q;  // output plane of O and LSE
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
@@ -281,8 +287,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             return false;
                         ptx::mbar_arrive_expect_tx_w(full, L::CHUNK_BYTES);
                         const uint32_t dst = s_ring + slot * L::CHUNK_BYTES;
-                        ptx::tma_load_3d_w(dst, map, full, ch * 128, j * L::BN, z_kv);
-                        ptx::tma_load_3d_w(dst + L::BOX_BYTES, map, full, ch * 128 + L::BOX_COLS, j * L::BN, z_kv);
+                        ptx::tma_load_3d_w(dst, map, full, ch * 128, (t0 + j) * L::BN, z_kv);
+                        ptx::tma_load_3d_w(dst + L::BOX_BYTES, map, full, ch * 128 + L::BOX_COLS, (t0 + j) * L::BN, z_kv);
                         armed_mask |= 1u << slot;
                         armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
                         if (++slot == NS) {
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 s[i] = __uint_as_float(sr[i]);
 
             // keys of this tile the row sees (>= 1): all < Skv, and (causal) <= the row itself
-            const int valid = (p.causal ? min(p.Skv, q0 + row + 1) : p.Skv) - j * L::BN;  // >= 1
+            const int valid = (p.causal ? min(p.Skv, q0 + row + 1) : p.Skv) - (t0 + j) * L::BN;  // >= 1
             if (valid < L::BN) {
 #pragma unroll
                 for (int i = 1; i < 128; ++i)
@@ -533,14 +539,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (p.lse != nullptr && q0 + row < p.Sq)
-                p.lse[static_cast<size_t>(z_q) * p.Sq + q0 + row] = (m_used + ptx::lg2(l)) * LN2;
+                p.lse[static_cast<size_t>(z_out) * p.Sq + q0 + row] = (m_used + ptx::lg2(l)) * LN2;
             ptx::fence_proxy_async_smem();
         }
         ptx::named_bar_sync(1, 128);
         if (threadIdx.x == 0 && !*abort_flag) {
 #pragma unroll
             for (int c2 = 0; c2 < D / L::BOX_COLS; ++c2)
-                ptx::tma_store_3d(&tm_o, s_q + c2 * L::BOX_BYTES, c2 * L::BOX_COLS, q0, z_q);
+                ptx::tma_store_3d(&tm_o, s_q + c2 * L::BOX_BYTES, c2 * L::BOX_COLS, q0, z_out);
             ptx::bulk_commit_group();
             ptx::bulk_wait_group_all();
         }

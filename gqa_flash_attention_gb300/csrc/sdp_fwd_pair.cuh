@@ -127,6 +127,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const bool leader = (rank == 0);
 
     int u = blockIdx.x;
+    // KV split (split-KV launches): the outermost unit coordinate.
+    const int units_per_split = static_cast<int>(gridDim.x) / p.kv_splits;
+    const int split = u / units_per_split;
+    u -= split * units_per_split;
     const int hi = u % p.G;
     u /= p.G;
     // Causal units do qt + 1 tiles: start the longest ones first.
@@ -138,7 +142,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int z_kv = bg;
     const int q0 = qt * L::BM;
     // Tiles this unit reads: all of them, or (causal) those holding keys <= its last row.
-    const int n = p.causal ? min(p.n_kvtiles, qt + 1) : p.n_kvtiles;
+    const int t0 = split * p.tiles_per_split;  // first KV tile of this unit
+    const int n = p.causal ? min(p.n_kvtiles, qt + 1) : min(p.n_kvtiles - t0, p.tiles_per_split);
+    const int z_out = split * p.planes_q + z_q;  // output plane of O and LSE
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
@@ -206,7 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
                     ptx::tma_load_3d_pair_w(dst + c * L::K_BOX_BYTES, &tm_k, full_l, c * 64,
-                                          j * L::BN + 64 * static_cast<int>(rank), z_kv);
+                                          (t0 + j) * L::BN + 64 * static_cast<int>(rank), z_kv);
                 return true;
             };
             auto load_v = [&](int j) -> bool {  // keys [j*128, +128), columns [rank*D/2, +D/2)
@@ -216,7 +222,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < D / 128; ++c)
                     ptx::tma_load_3d_pair_w(dst + c * L::V_BOX_BYTES, &tm_v, full_l,
-                                          static_cast<int>(rank) * (D / 2) + c * 64, j * L::BN, z_kv);
+                                          static_cast<int>(rank) * (D / 2) + c * 64, (t0 + j) * L::BN, z_kv);
                 return true;
             };
             bool ok = load_k(0);
@@ -325,7 +331,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 s[i] = __uint_as_float(sr[i]);
 
             // keys of this tile the row sees (>= 1): all < Skv, and (causal) <= the row itself
-            const int valid = (p.causal ? min(p.Skv, q0 + row + 1) : p.Skv) - j * L::BN;
+            const int valid = (p.causal ? min(p.Skv, q0 + row + 1) : p.Skv) - (t0 + j) * L::BN;
             if (valid < L::BN) {
 #pragma unroll
                 for (int i = 1; i < 128; ++i)
@@ -448,14 +454,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (p.lse != nullptr && q0 + row < p.Sq)
-                p.lse[static_cast<size_t>(z_q) * p.Sq + q0 + row] = (m_used + ptx::lg2(l)) * LN2;
+                p.lse[static_cast<size_t>(z_out) * p.Sq + q0 + row] = (m_used + ptx::lg2(l)) * LN2;
             ptx::fence_proxy_async_smem();
         }
         ptx::named_bar_sync(1, 128);
         if (threadIdx.x == 0 && !*abort_flag) {
 #pragma unroll
             for (int c2 = 0; c2 < D / 64; ++c2)
-                ptx::tma_store_3d(&tm_o, s_q + c2 * L::Q_BOX_BYTES, c2 * 64, q0, z_q);
+                ptx::tma_store_3d(&tm_o, s_q + c2 * L::Q_BOX_BYTES, c2 * 64, q0, z_out);
             ptx::bulk_commit_group();
             ptx::bulk_wait_group_all();
         }

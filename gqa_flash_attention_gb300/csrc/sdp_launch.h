@@ -17,6 +17,10 @@ struct KernelParams {
     unsigned long long timeout_ns;
     int debug_flags;
     int causal;  // row i sees keys 0..i only
+    // Split-KV launches: the grid is kv_splits copies of the unit grid, split s
+    // reading KV tiles [s * tiles_per_split, +tiles_per_split) and writing its
+    // partial O / LSE to output plane s * planes_q + (b, h). 1 / n_kvtiles otherwise.
+    int kv_splits, tiles_per_split, planes_q;
 };
 
 // Tensor maps of one launch: Q, K, V, O with 128-row boxes, and K with 64-row

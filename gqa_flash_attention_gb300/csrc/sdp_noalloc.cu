@@ -162,6 +162,9 @@ extern "C" int sdp_fwd_noalloc(const void *q, const void *k, const void *v, void
     p.timeout_ns = kTimeoutNs;
     p.debug_flags = 0;
     p.causal = 0;
+    p.kv_splits = 1;
+    p.tiles_per_split = static_cast<int>(n_kvtiles);
+    p.planes_q = static_cast<int>(planes_q);
 
     const int grid = static_cast<int>(units);
     cudaError_t e;

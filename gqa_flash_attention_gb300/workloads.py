@@ -35,6 +35,7 @@ class Workload:
     peaky_k: bool = False
     scale: float | None = None  # None means 1/sqrt(D)
     causal: bool = False        # row i sees keys 0..i
+    kv_splits: int = 1          # launch: split-KV run count (0 = automatic, 1 = none)
     note: str = field(default="", compare=False)
 
     @property
@@ -93,7 +94,18 @@ CAUSAL_WORKLOADS = {
     "mha_b4_s16k_d128_fp16_causal": WORKLOADS["mha_b4_s16k_d128_fp16"].with_(name="mha_b4_s16k_d128_fp16_causal",
                                                                              causal=True),
 }
-ALL_WORKLOADS = {**WORKLOADS, **CAUSAL_WORKLOADS}
+# Small-Sq shapes (the study's dispatch picks kernels by query length, with a
+# crossover at 16 rows): one-token decode over a long context, and 16 rows.
+# They run the split-KV forward with an automatic split count.
+DECODE_WORKLOADS = {
+    "gqa16_decode_b8_s16k_d256_fp16": Workload("gqa16_decode_b8_s16k_d256_fp16", 8, 32, 2, 1, 16384, 256, "fp16",
+                                               seed=8, kv_splits=0),
+    "gqa4_decode_b4_s32k_d128_bf16": Workload("gqa4_decode_b4_s32k_d128_bf16", 4, 32, 8, 1, 32768, 128, "bf16",
+                                              seed=9, kv_splits=0),
+    "gqa16_sq16_s16k_d256_fp16": Workload("gqa16_sq16_s16k_d256_fp16", 1, 32, 2, 16, 16384, 256, "fp16",
+                                          seed=10, kv_splits=0),
+}
+ALL_WORKLOADS = {**WORKLOADS, **CAUSAL_WORKLOADS, **DECODE_WORKLOADS}
 
 
 def _normal(rng: np.random.Generator, n: int) -> np.ndarray:

@@ -100,6 +100,47 @@ int sdp_merge(const void *o_parts, const float *lse_parts, int nparts, long long
               void *o, float *lse, void *stream);
 
 /*
+ * Split-KV forward, for problems with too few (batch, head, 128-row query
+ * tile) units to occupy the GPU: decode (Sq = 1 or a few rows) and short
+ * batches over long contexts. The "SyclKittens" summary's attention section
+ * (E.4) adds a split-K variant and its dispatch section (E.5) picks the
+ * kernel by query length and batch; here the keys are cut into n_splits
+ * contiguous runs of 128-key tiles, each (unit, run) pair becomes one CTA
+ * writing a partial O and LSE into the caller's workspace, and sdp_merge
+ * combines the runs into o / lse. The result is the same function as
+ * sdp_fwd's; the partial O is rounded to the I/O dtype once before the merge.
+ *
+ * sdp_fwd and sdp_fwd_splitkv both pack the G query heads of a KV group into
+ * one head of G * Sq rows when Sq is not a multiple of 128 (no causal mask):
+ * the same memory, viewed as [B, Hkv, G*Sq, D], so decode fills the tiles.
+ *
+ * sdp_fwd_splitkv_count — the split count a call with these sizes and
+ * n_splits uses on the current device: n_splits = 0 picks enough to give
+ * every SM a CTA; any request is clamped to [1, ceil(Skv / 128)] and evened
+ * out. Returns the count (>= 1) or a negative status code.
+ *
+ * sdp_fwd_splitkv_workspace_bytes — the workspace such a call needs (0 when
+ * the count is 1), or a negative status code.
+ *
+ * sdp_fwd_splitkv — sdp_fwd's arguments (no causal mask), plus
+ *   n_splits        0 (automatic) or the requested count
+ *   workspace       device scratch of at least the size above, 16-byte
+ *                   aligned, owned by the caller, not overlapping q/k/v/o;
+ *                   NULL allowed when the size is 0. Its contents on entry
+ *                   do not matter; on exit they are unspecified.
+ *   workspace_bytes its size
+ * Errors as sdp_fwd, plus SDP_ERR_INVALID_ARG for a negative n_splits or a
+ * missing / short / overlapping workspace. Two kernels are enqueued on
+ * `stream` (attention, then sdp_merge); the library allocates nothing but
+ * sdp_fwd's status word.
+ */
+int sdp_fwd_splitkv_count(int B, int Hq, int Hkv, int Sq, int Skv, int D, int dtype, int n_splits);
+long long sdp_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int D, int dtype, int n_splits);
+int sdp_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                    int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale, int dtype,
+                    int n_splits, void *workspace, unsigned long long workspace_bytes, void *stream);
+
+/*
  * sdp_fwd_noalloc — sdp_fwd for callers that cannot allocate device memory.
  * The paper has no counterpart: this is a library-usage variant, not a step of
  * the method.
@@ -163,7 +204,8 @@ unsigned int sdp_set_wait_timeout_ms(unsigned int ms);
  * no copies at all, so every consumer wait runs out and the kernel returns
  * through its timeout path (used to test that path without a fault). Bit 1:
  * always run the single-CTA kernel, never the CTA-pair kernel (both compute
- * the same result; tests compare them). Returns the previous flags.
+ * the same result; tests compare them). Bit 2: never pack the query heads of
+ * a group into one head (same result; tests compare). Returns the previous flags.
  */
 int sdp_set_debug_flags(int flags);
 
@@ -173,7 +215,7 @@ int sdp_last_cuda_error(void);
 /* A static, human-readable description of a status code. */
 const char *sdp_strerror(int code);
 
-/* ABI version: 100 * major + minor (101: sdp_fwd_causal; 102: sdp_merge). */
+/* ABI version: 100 * major + minor (101: sdp_fwd_causal; 102: sdp_merge; 103: split-KV). */
 int sdp_version(void);
 
 /* Free the per-device status words. Call only with no sdp work in flight. */

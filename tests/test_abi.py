@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_version_and_messages(L):
-    assert L.sdp_version() == 102
+    assert L.sdp_version() == 103
     for code in range(-6, 1):
         assert len(sdp.strerror(code)) > 0
     assert sdp.strerror(-99) == "unknown status code"
@@ -92,3 +92,37 @@ def test_python_binding_rejects_bad_tensors():
         sdp.sdp_fwd(q, q, q)  # CPU tensors
     with pytest.raises(ValueError):
         sdp.sdp_fwd(q[0], q, q)  # not 4-D
+
+
+def split_call(**kw):
+    args = dict(q=A, k=2 * A, v=3 * A, o=4 * A, lse=5 * A, B=1, Hq=4, Hkv=1, Sq=1, Skv=1000, D=128,
+                scale=0.088, dtype=sdp.SDP_FP16, n_splits=0, workspace=6 * A, workspace_bytes=1 << 20)
+    args.update(kw)
+    return sdp.sdp_fwd_splitkv_ptr(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=64), sdp.SDP_ERR_UNSUPPORTED),
+    (dict(dtype=2), sdp.SDP_ERR_UNSUPPORTED),
+    (dict(q=0), sdp.SDP_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), sdp.SDP_ERR_INVALID_ARG),
+    (dict(Skv=0), sdp.SDP_ERR_INVALID_ARG),
+    (dict(scale=math.nan), sdp.SDP_ERR_INVALID_ARG),
+    (dict(o=A), sdp.SDP_ERR_INVALID_ARG),
+    (dict(n_splits=-1), sdp.SDP_ERR_INVALID_ARG),
+    (dict(k=2 * A + 4), sdp.SDP_ERR_ALIGNMENT),
+])
+def test_split_kv_validation_errors_launch_nothing(L, kw, code):
+    assert split_call(**kw) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 4, 1, 1, 1000, 64, 0, 0), sdp.SDP_ERR_UNSUPPORTED),
+    ((1, 4, 1, 1, 1000, 128, 5, 0), sdp.SDP_ERR_UNSUPPORTED),
+    ((0, 4, 1, 1, 1000, 128, 0, 0), sdp.SDP_ERR_INVALID_ARG),
+    ((1, 6, 4, 1, 1000, 128, 0, 0), sdp.SDP_ERR_INVALID_ARG),
+    ((1, 4, 1, 1, 1000, 128, 0, -2), sdp.SDP_ERR_INVALID_ARG),
+])
+def test_split_kv_planning_rejects_bad_sizes(L, args, code):
+    assert L.sdp_fwd_splitkv_count(*args) == code
+    assert L.sdp_fwd_splitkv_workspace_bytes(*args) == code
