@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--op", choices=["attention", "merge"], default="attention",
                     help="merge: time sdp_merge (HBM-bound) on a context-parallel-shaped case instead")
     ap.add_argument("--merge-parts", type=int, default=8)
+    ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
+                    help="replay each step from a CUDA graph (auto: for the split-KV decode workloads, whose "
+                         "steps are shorter than the host's per-call work)")
     return ap.parse_args()
 
 
@@ -294,6 +297,15 @@ def ours_arm(args, w):
     torch.cuda.synchronize(dev)
     if sdp.poll_status() != sdp.SDP_OK:
         raise RuntimeError("kernel reported a timeout during warm-up")
+    use_graph = args.graph == "on" or (args.graph == "auto" and w.kv_splits != 1)
+    step = call
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        step = graph.replay
 
     K = args.steps
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -307,7 +319,7 @@ def ours_arm(args, w):
         if flush is not None:
             flush.zero_()
         ev0[i].record(stream)
-        call()
+        step()
         ev1[i].record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -393,10 +405,12 @@ def ours_arm(args, w):
                "sample": f"{nrows} query rows per (batch, head) x {w.B * w.Hq} heads of {w.name}, all {w.Skv} "
                          f"keys ({sec:.1f} s)"}
 
+    cfg = config_of(w, world)
+    cfg["cuda_graph"] = use_graph
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic", "config": config_of(w, world),
+        "dtype": w.dtype, "data": "synthetic", "config": cfg,
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
         "gpu_launches": K * launches_per_step,

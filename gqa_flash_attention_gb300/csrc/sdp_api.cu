@@ -165,14 +165,15 @@ int shape_of(int B, int Hq, int Hkv, int Sq, int Skv, int causal, Shape *sh)
     return SDP_OK;
 }
 
-// Split count for a split-KV call: `requested` (0 = enough units to cover the
-// SMs once), clamped to [1, KV tiles], then evened out so that every split
+// Split count for a split-KV call: `requested` (0 = as many as fit the SMs in
+// one wave: one CTA per SM, so a second, mostly empty wave would add a whole
+// run's time), clamped to [1, KV tiles], then evened out so that every split
 // reads the same number of tiles except a shorter last one.
 int set_splits(Shape *sh, int requested, int sms)
 {
     long long s = requested;
     if (s <= 0)
-        s = sh->units >= sms ? 1 : (sms + sh->units - 1) / sh->units;
+        s = sh->units >= sms ? 1 : sms / sh->units;
     s = s < 1 ? 1 : (s > sh->n_kvtiles ? sh->n_kvtiles : s);
     const long long tps = (sh->n_kvtiles + s - 1) / s;
     s = (sh->n_kvtiles + tps - 1) / tps;

@@ -22,7 +22,7 @@
 
 namespace {
 
-constexpr int kWarpsPerBlock = 8;
+constexpr int kWarpsPerBlock = 4;
 
 template <bool BF16>
 __device__ __forceinline__ float2 unpack2(uint32_t u)
@@ -50,6 +50,42 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 
 // W 32-bit words (2*W elements) per lane: W = D / 64.
 template <int D, bool BF16>
+__device__ __forceinline__ void accumulate(float *acc, const uint32_t *words, float w)
+{
+#pragma unroll
+    for (int i = 0; i < D / 64; ++i) {
+        const float2 f = unpack2<BF16>(words[i]);
+        acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+    }
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void store_row(uint16_t *o, float *lse, long long r, int lane, const float *acc,
+                                          float lse_r)
+{
+    constexpr int W = D / 64;
+    using Vec = typename std::conditional<W == 4, uint4, uint2>::type;
+    Vec out;
+    uint32_t *ow = reinterpret_cast<uint32_t *>(&out);
+#pragma unroll
+    for (int i = 0; i < W; ++i)
+        ow[i] = pack2<BF16>(acc[2 * i], acc[2 * i + 1]);
+    reinterpret_cast<Vec *>(o)[r * 32 + lane] = out;
+    if (lse != nullptr && lane == 0)
+        lse[r] = lse_r;
+}
+
+// One warp per row. With up to kFastParts parts every load of a row (the
+// part rows and lane p's part LSE) is issued at once: the split-KV merge of a
+// decode step has few rows and is bound by that one round trip. Beyond that,
+// the part LSEs are read once (lane p holds part p's while P <= 32) and the
+// part rows kMaxInFlight at a time; the context-parallel merge of long
+// sequences is bound by HBM bandwidth either way.
+constexpr int kMaxInFlight = 8;
+constexpr int kFastParts = 16;  // up to this many parts, one round trip per row
+
+template <int D, bool BF16>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     merge_kernel(const uint16_t *__restrict__ o_parts, const float *__restrict__ lse_parts, int P, long long rows,
                  uint16_t *__restrict__ o, float *__restrict__ lse)
@@ -61,70 +97,83 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     if (r >= rows)
         return;
 
-    // Row log-sum-exp over the parts: max, then sum of exp relative to it.
-    float m = -INFINITY;
-    for (int p = lane; p < P; p += 32)
-        m = fmaxf(m, lse_parts[static_cast<long long>(p) * rows + r]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    float sum = 0.f;
-    for (int p = lane; p < P; p += 32)
-        sum += expf(lse_parts[static_cast<long long>(p) * rows + r] - m);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    const float lse_r = m + logf(sum);
-
+    const Vec *src = reinterpret_cast<const Vec *>(o_parts) + r * 32 + lane;
+    const long long part_stride = rows * 32;  // in Vec units
     float acc[2 * W];
 #pragma unroll
     for (int i = 0; i < 2 * W; ++i)
         acc[i] = 0.f;
-    const Vec *src = reinterpret_cast<const Vec *>(o_parts) + r * 32 + lane;
-    const long long part_stride = rows * 32;  // in Vec units
+
+    if (P <= kFastParts) {
+        // Few parts (the split-KV merge of a decode step): every load of the
+        // row is issued before the reductions, one memory round trip in all.
+        Vec v[kFastParts];
+#pragma unroll
+        for (int u = 0; u < kFastParts; ++u)
+            if (u < P)
+                v[u] = __ldg(src + static_cast<long long>(u) * part_stride);
+        const float l = lane < P ? __ldg(lse_parts + static_cast<long long>(lane) * rows + r) : -INFINITY;
+        float m = l;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const float e = lane < P ? expf(l - m) : 0.f;
+        float sum = e;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        const float w_l = e / sum;
+#pragma unroll
+        for (int u = 0; u < kFastParts; ++u) {
+            const float w = __shfl_sync(0xffffffffu, w_l, u);
+            if (u < P)
+                accumulate<D, BF16>(acc, reinterpret_cast<const uint32_t *>(&v[u]), w);
+        }
+        store_row<D, BF16>(o, lse, r, lane, acc, m + logf(sum));
+        return;
+    }
+
+    // Row log-sum-exp over the parts: max, then sum of exp relative to it.
+    // The first 32 part LSEs stay in a register (lane p: part p).
+    const float l0 = lane < P ? __ldg(lse_parts + static_cast<long long>(lane) * rows + r) : -INFINITY;
+    float m = l0;
+    for (int p = lane + 32; p < P; p += 32)
+        m = fmaxf(m, __ldg(lse_parts + static_cast<long long>(p) * rows + r));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float e0 = lane < P ? expf(l0 - m) : 0.f;
+    float sum = e0;
+    for (int p = lane + 32; p < P; p += 32)
+        sum += expf(__ldg(lse_parts + static_cast<long long>(p) * rows + r) - m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const float lse_r = m + logf(sum);
+    const float inv_sum = 1.f / sum;
+
     for (int p0 = 0; p0 < P; p0 += 32) {
         // weight of part p0 + lane, broadcast below
         const int pl = p0 + lane;
-        const float w_l = pl < P ? expf(lse_parts[static_cast<long long>(pl) * rows + r] - lse_r) : 0.f;
+        const float w_l = p0 == 0 ? e0 * inv_sum
+                                  : (pl < P ? expf(__ldg(lse_parts + static_cast<long long>(pl) * rows + r) - lse_r)
+                                            : 0.f);
         const int pend = min(32, P - p0);
-        int q = 0;
-        for (; q + 4 <= pend; q += 4) {  // four loads in flight
-            Vec v[4];
+        for (int q = 0; q < pend; q += kMaxInFlight) {
+            Vec v[kMaxInFlight];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                v[u] = __ldg(src + static_cast<long long>(p0 + q + u) * part_stride);
+            for (int u = 0; u < kMaxInFlight; ++u)
+                if (q + u < pend)
+                    v[u] = __ldg(src + static_cast<long long>(p0 + q + u) * part_stride);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float w = __shfl_sync(0xffffffffu, w_l, q + u);
-                const uint32_t *words = reinterpret_cast<const uint32_t *>(&v[u]);
-#pragma unroll
-                for (int i = 0; i < W; ++i) {
-                    const float2 f = unpack2<BF16>(words[i]);
-                    acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
-                    acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
-                }
-            }
-        }
-        for (; q < pend; ++q) {
-            const Vec v = __ldg(src + static_cast<long long>(p0 + q) * part_stride);
-            const float w = __shfl_sync(0xffffffffu, w_l, q);
-            const uint32_t *words = reinterpret_cast<const uint32_t *>(&v);
-#pragma unroll
-            for (int i = 0; i < W; ++i) {
-                const float2 f = unpack2<BF16>(words[i]);
-                acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
-                acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+            for (int u = 0; u < kMaxInFlight; ++u) {
+                const float w = __shfl_sync(0xffffffffu, w_l, (q + u) & 31);
+                if (q + u < pend)
+                    accumulate<D, BF16>(acc, reinterpret_cast<const uint32_t *>(&v[u]), w);
             }
         }
     }
-    Vec out;
-    uint32_t *ow = reinterpret_cast<uint32_t *>(&out);
-#pragma unroll
-    for (int i = 0; i < W; ++i)
-        ow[i] = pack2<BF16>(acc[2 * i], acc[2 * i + 1]);
-    reinterpret_cast<Vec *>(o)[r * 32 + lane] = out;
-    if (lse != nullptr && lane == 0)
-        lse[r] = lse_r;
+    store_row<D, BF16>(o, lse, r, lane, acc, lse_r);
 }
 
 template <int D, bool BF16>
@@ -132,7 +181,7 @@ cudaError_t launch(const void *o_parts, const float *lse_parts, int P, long long
                    cudaStream_t st)
 {
     const long long blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    merge_kernel<D, BF16><<<static_cast<unsigned>(blocks), 32 * kWarpsPerBlock, 0, st>>>(
+merge_kernel<D, BF16><<<static_cast<unsigned>(blocks), 32 * kWarpsPerBlock, 0, st>>>(
         static_cast<const uint16_t *>(o_parts), lse_parts, P, rows, static_cast<uint16_t *>(o), lse);
     return cudaGetLastError();
 }

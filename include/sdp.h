@@ -115,9 +115,9 @@ int sdp_merge(const void *o_parts, const float *lse_parts, int nparts, long long
  * the same memory, viewed as [B, Hkv, G*Sq, D], so decode fills the tiles.
  *
  * sdp_fwd_splitkv_count — the split count a call with these sizes and
- * n_splits uses on the current device: n_splits = 0 picks enough to give
- * every SM a CTA; any request is clamped to [1, ceil(Skv / 128)] and evened
- * out. Returns the count (>= 1) or a negative status code.
+ * n_splits uses on the current device: n_splits = 0 picks the most that
+ * still run in one wave of one CTA per SM; any request is clamped to
+ * [1, ceil(Skv / 128)] and evened out. Returns the count (>= 1) or a negative status code.
  *
  * sdp_fwd_splitkv_workspace_bytes — the workspace such a call needs (0 when
  * the count is 1), or a negative status code.

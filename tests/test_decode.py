@@ -131,11 +131,12 @@ def test_split_kv_single_cta(w, splits):
 def test_split_counts_and_workspace_sizes():
     fp16 = sdp.SDP_FP16
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # decode, 32 heads over 2 KV heads: packed into 2 units, auto covers the SMs
+    # decode, 32 heads over 2 KV heads: packed into 2 units, auto fills one wave
     n_kv = (16384 + 127) // 128
     s = sdp.splitkv_count(1, 32, 2, 1, 16384, 256, fp16, 0)
-    tps = -(-n_kv // -(-sms // 2))
+    tps = -(-n_kv // (sms // 2))
     assert s == -(-n_kv // tps)
+    assert 2 * s <= sms
     assert sdp.splitkv_workspace_bytes(1, 32, 2, 1, 16384, 256, fp16, 0) == \
         -(-(s * 32 * 256 * 2) // 256) * 256 + s * 32 * 4
     # requests clamp to the KV tile count and even out
