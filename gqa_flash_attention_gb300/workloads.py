@@ -108,6 +108,98 @@ DECODE_WORKLOADS = {
 ALL_WORKLOADS = {**WORKLOADS, **CAUSAL_WORKLOADS, **DECODE_WORKLOADS}
 
 
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """A batch of sequences of different lengths packed back to back.
+
+    Sequence b has lens_q[b] query rows and lens_k[b] key rows; Q is
+    [total_q, Hq, D] and K, V are [total_k, Hkv, D] (token, head, dim).
+    """
+    name: str
+    lens_q: tuple
+    lens_k: tuple
+    Hq: int
+    Hkv: int
+    D: int
+    dtype: str = "fp16"
+    seed: int = 0
+    scale: float | None = None
+    causal: bool = False
+    note: str = field(default="", compare=False)
+
+    @property
+    def nseq(self) -> int:
+        return len(self.lens_q)
+
+    @property
+    def total_q(self) -> int:
+        return int(sum(self.lens_q))
+
+    @property
+    def total_k(self) -> int:
+        return int(sum(self.lens_k))
+
+    @property
+    def max_q(self) -> int:
+        return int(max(self.lens_q))
+
+    @property
+    def cu_q(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.lens_q)]).astype(np.int32)
+
+    @property
+    def cu_k(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.lens_k)]).astype(np.int32)
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.D) if self.scale is None else float(self.scale)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return DTYPES[self.dtype]
+
+    def flops(self) -> int:
+        """4 * D FLOPs per (query head, query row, key the row sees)."""
+        seen = 0
+        for lq, lk in zip(self.lens_q, self.lens_k):
+            if not self.causal:
+                seen += lq * lk
+            else:
+                full = min(lq, lk)
+                seen += full * (full + 1) // 2 + (lq - full) * lk
+        return 4 * self.Hq * self.D * seen
+
+    def hbm_bytes(self) -> int:
+        q = self.total_q * self.Hq * self.D * 2
+        kv = 2 * self.total_k * self.Hkv * self.D * 2
+        return 2 * q + kv + self.total_q * self.Hq * 4
+
+
+def varlen_lengths(n: int, lo: int, hi: int, seed: int) -> tuple:
+    """n lengths, log-uniform in [lo, hi] (PCG64, seeded), as a tuple of ints."""
+    rng = np.random.default_rng(seed)
+    x = np.exp(rng.uniform(math.log(lo), math.log(hi), size=n))
+    return tuple(int(round(t)) for t in x)
+
+
+_VL_A = varlen_lengths(12, 256, 16384, seed=11)
+_VL_B = varlen_lengths(24, 64, 8192, seed=12)
+# Packed prefill batches: a long-tailed mix of sequence lengths (log-uniform),
+# so most sequences end inside a 128-row tile. Self-attention (keys =
+# queries) on the headline head layout, and a bf16 batch whose key lengths
+# (history + chunk) exceed the query lengths.
+VARLEN_WORKLOADS = {
+    "varlen12_gqa16_d256_fp16": VarlenWorkload("varlen12_gqa16_d256_fp16", _VL_A, _VL_A, 32, 2, 256, "fp16",
+                                               seed=11),
+    "varlen12_gqa16_d256_fp16_causal": VarlenWorkload("varlen12_gqa16_d256_fp16_causal", _VL_A, _VL_A, 32, 2, 256,
+                                                      "fp16", seed=11, causal=True),
+    "varlen24_gqa4_d128_bf16": VarlenWorkload("varlen24_gqa4_d128_bf16", _VL_B,
+                                              tuple(x + y for x, y in zip(_VL_B, varlen_lengths(24, 1, 4096, 13))),
+                                              32, 8, 128, "bf16", seed=12),
+}
+
+
 def _normal(rng: np.random.Generator, n: int) -> np.ndarray:
     out = np.empty(n, dtype=np.float32)
     step = 1 << 26
@@ -162,3 +254,17 @@ def sample_rows(w: Workload, n: int = 256, seed: int | None = None) -> np.ndarra
             rows = np.concatenate([[0], np.sort(mid), [w.Sq - 1]])[:m]
             out[b, h] = np.sort(rows).astype(np.int32)
     return out
+
+
+def make_varlen_inputs(w: VarlenWorkload):
+    """(q, k, v) as contiguous CPU tensors of the workload's dtype, packed
+    (token, head, dim): q [total_q, Hq, D], k and v [total_k, Hkv, D]; same
+    recipe as make_inputs. The sequence offsets are w.cu_q and w.cu_k."""
+    rng = np.random.default_rng(w.seed)
+    q = _normal(rng, w.total_q * w.Hq * w.D)
+    k = _normal(rng, w.total_k * w.Hkv * w.D)
+    v = _normal(rng, w.total_k * w.Hkv * w.D)
+    q = _round(q, w.dtype).reshape(w.total_q, w.Hq, w.D)
+    k = _round(k, w.dtype).reshape(w.total_k, w.Hkv, w.D)
+    v = _round(v, w.dtype).reshape(w.total_k, w.Hkv, w.D)
+    return q, k, v

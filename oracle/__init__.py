@@ -54,6 +54,9 @@ def _load():
         lib.oracle_sdp_row_probs.argtypes = [p, p, p, i, i, i, i, i, i, i, ctypes.c_double, i,
                                              i, i, i, p, p, p]
         lib.oracle_sdp_row_probs.restype = i
+        lib.oracle_sdp_fwd_varlen.argtypes = [p, p, p, i, i, i, i, i, ctypes.c_double, i, p, p,
+                                              ctypes.c_long, ctypes.c_long, p, p]
+        lib.oracle_sdp_fwd_varlen.restype = i
         lib.oracle_fp16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_fp16_to_double.restype = ctypes.c_double
         lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -156,4 +159,30 @@ def sdp_merge(o_parts, lse_parts):
     rc = _load().oracle_sdp_merge(_ptr(op), _ptr(lp), int(P), int(rows), int(D), _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle rejected the merge sizes")
+    return o, lse
+
+
+def sdp_fwd_varlen(q, k, v, dtype: int, cu_q, cu_k, scale: float, causal: bool = False):
+    """Attention over a variable-length batch packed back to back (fp64).
+
+    q: [total_q, Hq, D], k/v: [total_k, Hkv, D] 16-bit patterns (or fp16/bf16
+    tensors); cu_q, cu_k: int32 [nseq + 1] sequence offsets. Sequence b's query
+    rows attend to its own keys only (causal: its keys 0..i). Returns
+    (o [total_q, Hq, D], lse [Hq, total_q]); a row that sees no key has O = 0
+    and LSE = -inf.
+    """
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    total_q, Hq, D = (int(x) for x in q.shape)
+    total_k, Hkv = int(k.shape[0]), int(k.shape[1])
+    assert tuple(k.shape) == tuple(v.shape) and int(k.shape[2]) == D
+    cq = np.ascontiguousarray(np.asarray(cu_q, dtype=np.int32))
+    ck = np.ascontiguousarray(np.asarray(cu_k, dtype=np.int32))
+    assert cq.ndim == 1 and cq.shape == ck.shape
+    o = np.empty((total_q, Hq, D), dtype=np.float64)
+    lse = np.empty((Hq, total_q), dtype=np.float64)
+    rc = _load().oracle_sdp_fwd_varlen(_ptr(qb), _ptr(kb), _ptr(vb), int(dtype), int(cq.size - 1), Hq, Hkv, D,
+                                       float(scale), int(bool(causal)), _ptr(cq), _ptr(ck), total_q, total_k,
+                                       _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes or sequence offsets")
     return o, lse

@@ -261,6 +261,104 @@ int oracle_sdp_row_probs(const uint16_t *q, const uint16_t *k, const uint16_t *v
 }
 
 /*
+ * Variable-length batch: sequences of different lengths packed back to back
+ * (no counterpart on the pages; the plain generalisation of the ragged last
+ * tile of one sequence to a batch of ragged sequences). Sequence b owns query
+ * rows [cu_q[b], cu_q[b+1]) and key rows [cu_k[b], cu_k[b+1]); each of its
+ * query rows attends to that sequence's keys only, by the definition at the
+ * top of this file with Sq = len_q(b) and Skv = len_k(b) (causal: row i of the
+ * sequence sees the sequence's keys 0..i). A row that sees no key (a
+ * sequence with no keys) has O = 0 and LSE = -inf.
+ *
+ * Layout (token, head, dim), contiguous 16-bit patterns:
+ *   Q [total_q, Hq, D], K and V [total_k, Hkv, D];
+ *   o_out double [total_q, Hq, D]; lse_out double [Hq, total_q] (may be NULL).
+ * cu_q, cu_k: int32 [nseq + 1], cu[0] = 0, non-decreasing, cu[nseq] = total.
+ * Returns 0, or -1 on bad sizes or offsets.
+ */
+int oracle_sdp_fwd_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype, int nseq,
+                          int Hq, int Hkv, int D, double scale, int causal, const int32_t *cu_q,
+                          const int32_t *cu_k, long total_q, long total_k, double *o_out, double *lse_out)
+{
+    if (nseq <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0 || total_q < 0 || total_k < 0)
+        return -1;
+    if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16)
+        return -1;
+    if (cu_q[0] != 0 || cu_k[0] != 0 || cu_q[nseq] != total_q || cu_k[nseq] != total_k)
+        return -1;
+    int max_k = 0;
+    for (int b = 0; b < nseq; ++b) {
+        if (cu_q[b + 1] < cu_q[b] || cu_k[b + 1] < cu_k[b])
+            return -1;
+        if (cu_k[b + 1] - cu_k[b] > max_k)
+            max_k = cu_k[b + 1] - cu_k[b];
+    }
+    const int G = Hq / Hkv;
+    const size_t kv_elems = (size_t)(max_k > 0 ? max_k : 1) * D;
+    double *Kg = (double *)malloc(sizeof(double) * kv_elems);
+    double *Vg = (double *)malloc(sizeof(double) * kv_elems);
+    if (!Kg || !Vg) {
+        free(Kg);
+        free(Vg);
+        return -1;
+    }
+    int status = 0;
+    for (int b = 0; b < nseq && !status; ++b) {
+        const int row_q = cu_q[b], len_q = cu_q[b + 1] - cu_q[b];
+        const int row_k = cu_k[b], len_k = cu_k[b + 1] - cu_k[b];
+        for (int g = 0; g < Hkv && !status; ++g) {
+            /* this sequence's keys and values of KV head g, row j at Kg + j*D */
+#pragma omp parallel for schedule(static)
+            for (long t = 0; t < (long)len_k * D; ++t) {
+                const size_t src = ((size_t)(row_k + t / D) * Hkv + g) * D + t % D;
+                Kg[t] = decode(k[src], dtype);
+                Vg[t] = decode(v[src], dtype);
+            }
+            const long npairs = (long)G * len_q;
+#pragma omp parallel
+            {
+                double *qrow = (double *)malloc(sizeof(double) * D);
+                double *s = (double *)malloc(sizeof(double) * (len_k > 0 ? len_k : 1));
+                double *p = (double *)malloc(sizeof(double) * (len_k > 0 ? len_k : 1));
+                int ok = qrow && s && p;
+                if (!ok) {
+#pragma omp atomic write
+                    status = -1;
+                }
+#pragma omp for schedule(dynamic, 4)
+                for (long t = 0; t < npairs; ++t) {
+                    if (!ok)
+                        continue;
+                    const int h = g * G + (int)(t / len_q);
+                    const int i = (int)(t % len_q);
+                    const size_t at = ((size_t)(row_q + i) * Hq + h) * D;
+                    double *o = o_out + at;
+                    const int seen = (causal && i + 1 < len_k) ? i + 1 : len_k;
+                    double lse;
+                    if (seen == 0) {
+                        for (int d = 0; d < D; ++d)
+                            o[d] = 0.0;
+                        lse = -INFINITY;
+                    } else {
+                        for (int d = 0; d < D; ++d)
+                            qrow[d] = decode(q[at + d], dtype);
+                        attend_row(qrow, Kg, Vg, seen, D, scale, s, p, o, &lse);
+                    }
+                    if (lse_out)
+                        lse_out[(size_t)h * total_q + row_q + i] = lse;
+                }
+                free(qrow);
+                free(s);
+                free(p);
+            }
+        }
+    }
+    free(Kg);
+    free(Vg);
+    return status;
+}
+
+/*
  * Merge of partial attention results over disjoint key sets — the state
  * exchange of ring / context-parallel attention ("SyclKittens" summary,
  * section I.2: each step merges the online-softmax state of the next key

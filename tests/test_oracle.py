@@ -364,3 +364,82 @@ def test_merge_closed_forms():
     o, lse = oracle.sdp_merge(parts[:2], two_l)
     assert np.abs(o - (0.25 * parts[0] + 0.75 * parts[1])).max() <= 1e-14
     assert np.abs(lse - math.log(4.0)).max() <= 1e-14
+
+
+# ------------------------------------------------------- variable length
+
+def rand_thd(lens_q, lens_k, Hq, Hkv, D, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(sum(lens_q), Hq, D, generator=g).to(TD[dtype])
+    k = torch.randn(sum(lens_k), Hkv, D, generator=g).to(TD[dtype])
+    v = torch.randn(sum(lens_k), Hkv, D, generator=g).to(TD[dtype])
+    cu = lambda ls: np.concatenate([[0], np.cumsum(ls)]).astype(np.int32)  # noqa: E731
+    return q, k, v, cu(lens_q), cu(lens_k)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_single_sequence_equals_dense_layout(causal):
+    """One sequence in (token, head, dim) layout is the dense [1, H, S, D] case transposed."""
+    q, k, v, cq, ck = rand_thd([37], [53], 4, 2, 16, FP16, seed=71)
+    o, lse = oracle.sdp_fwd_varlen(q, k, v, FP16, cq, ck, 0.3, causal=causal)
+    qd, kd, vd = (t.permute(1, 0, 2).unsqueeze(0).contiguous() for t in (q, k, v))
+    od, lsed = oracle.sdp_fwd(qd, kd, vd, FP16, (1, 4, 2, 37, 53, 16), 0.3, causal=causal)
+    assert np.array_equal(o, od[0].transpose(1, 0, 2))
+    assert np.array_equal(lse, lsed[0])
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_matches_torch_float64_per_sequence(dtype, causal):
+    lens_q, lens_k = [5, 1, 17, 9], [12, 3, 17, 2]
+    Hq, Hkv, D = 4, 2, 16
+    q, k, v, cq, ck = rand_thd(lens_q, lens_k, Hq, Hkv, D, dtype, seed=72 + causal)
+    scale = 0.7 / math.sqrt(D)
+    o, lse = oracle.sdp_fwd_varlen(q, k, v, dtype, cq, ck, scale, causal=causal)
+    G = Hq // Hkv
+    for b in range(len(lens_q)):
+        qs = q[cq[b]:cq[b + 1]].double().permute(1, 0, 2)
+        ks = k[ck[b]:ck[b + 1]].double().permute(1, 0, 2).repeat_interleave(G, dim=0)
+        vs = v[ck[b]:ck[b + 1]].double().permute(1, 0, 2).repeat_interleave(G, dim=0)
+        ref = F.scaled_dot_product_attention(qs, ks, vs, scale=scale, is_causal=causal)
+        s = qs @ ks.transpose(-1, -2) * scale
+        if causal:
+            s = s.masked_fill(~torch.ones(lens_q[b], lens_k[b], dtype=torch.bool).tril(), float("-inf"))
+        ref_lse = torch.logsumexp(s, dim=-1)
+        assert np.abs(o[cq[b]:cq[b + 1]] - ref.permute(1, 0, 2).numpy()).max() <= 1e-12
+        assert np.abs(lse[:, cq[b]:cq[b + 1]] - ref_lse.numpy()).max() <= 1e-12
+
+
+def test_varlen_sequence_without_keys_gives_zero_and_minus_inf():
+    q, k, v, cq, ck = rand_thd([3, 4, 2], [6, 0, 5], 2, 1, 8, FP16, seed=74)
+    o, lse = oracle.sdp_fwd_varlen(q, k, v, FP16, cq, ck, 0.5)
+    assert np.array_equal(o[3:7], np.zeros((4, 2, 8)))
+    assert np.all(np.isneginf(lse[:, 3:7]))
+    assert np.all(np.isfinite(lse[:, :3])) and np.all(np.isfinite(lse[:, 7:]))
+
+
+def test_varlen_sequences_do_not_see_each_other():
+    """Changing one sequence's keys and values leaves every other sequence's rows as they were,
+    and a sequence with no query rows contributes nothing."""
+    q, k, v, cq, ck = rand_thd([4, 6, 3], [5, 7, 4], 4, 1, 8, BF16, seed=75)
+    o1, l1 = oracle.sdp_fwd_varlen(q, k, v, BF16, cq, ck, 0.4)
+    k2, v2 = k.clone(), v.clone()
+    k2[5:12] = torch.randn(7, 1, 8).to(torch.bfloat16)
+    v2[5:12] = torch.randn(7, 1, 8).to(torch.bfloat16)
+    o2, l2 = oracle.sdp_fwd_varlen(q, k2, v2, BF16, cq, ck, 0.4)
+    keep = np.r_[0:4, 10:13]
+    assert np.array_equal(o1[keep], o2[keep]) and np.array_equal(l1[:, keep], l2[:, keep])
+    assert not np.array_equal(o1[4:10], o2[4:10])
+    # insert an empty-query sequence with its own keys between sequences 0 and 1
+    kx = torch.cat([k[:5], torch.randn(3, 1, 8).to(torch.bfloat16), k[5:]])
+    vx = torch.cat([v[:5], torch.randn(3, 1, 8).to(torch.bfloat16), v[5:]])
+    o3, l3 = oracle.sdp_fwd_varlen(q, kx, vx, BF16, np.array([0, 4, 4, 10, 13], np.int32),
+                                   np.array([0, 5, 8, 15, 19], np.int32), 0.4)
+    assert np.array_equal(o1, o3) and np.array_equal(l1, l3)
+
+
+def test_varlen_rejects_bad_offsets():
+    q, k, v, cq, ck = rand_thd([3, 4], [3, 4], 2, 1, 8, FP16, seed=76)
+    for bad_q, bad_k in [([1, 3, 7], ck), ([0, 5, 4], ck), ([0, 3, 6], ck), (cq, [0, 3, 8])]:
+        with pytest.raises(ValueError):
+            oracle.sdp_fwd_varlen(q, k, v, FP16, np.array(bad_q, np.int32), np.array(bad_k, np.int32), 0.5)

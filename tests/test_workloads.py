@@ -74,3 +74,25 @@ def test_causal_flop_count():
     assert w.flops() == 4 * 128 * (1 + 2 + 3 + 3 + 3)
     w2 = Workload("c2", 2, 4, 2, 300, 300, 64, causal=True)
     assert w2.flops() == 4 * 64 * 2 * 4 * (300 * 301 // 2)
+
+
+def test_varlen_workloads_offsets_and_flops():
+    for w in workloads.VARLEN_WORKLOADS.values():
+        assert w.cu_q[0] == 0 and w.cu_q[-1] == w.total_q and np.all(np.diff(w.cu_q) == np.array(w.lens_q))
+        assert w.cu_k[-1] == w.total_k and len(w.lens_k) == w.nseq
+        seen = 0
+        for lq, lk in zip(w.lens_q, w.lens_k):
+            if w.causal:
+                seen += sum(min(i + 1, lk) for i in range(lq))
+            else:
+                seen += lq * lk
+        assert w.flops() == 4 * w.Hq * w.D * seen
+
+
+def test_varlen_inputs_are_seeded_and_shaped():
+    w = workloads.VarlenWorkload("t", (3, 130), (5, 1), 4, 2, 128, "bf16", seed=9)
+    q, k, v = workloads.make_varlen_inputs(w)
+    assert q.shape == (133, 4, 128) and k.shape == (6, 2, 128) and v.shape == k.shape
+    assert q.dtype == torch.bfloat16
+    q2, _, _ = workloads.make_varlen_inputs(w)
+    assert torch.equal(q, q2)
