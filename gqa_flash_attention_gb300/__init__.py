@@ -30,6 +30,7 @@ SDP_ERR_ALIGNMENT = -3
 SDP_ERR_OVERFLOW = -4
 SDP_ERR_CUDA = -5
 SDP_ERR_DEVICE_TIMEOUT = -6
+SDP_ERR_BAD_SEQLENS = -7
 
 _DTYPE_CODE = {torch.float16: SDP_FP16, torch.bfloat16: SDP_BF16}
 
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.sdp_fwd_causal.restype = i
         L.sdp_merge.argtypes = [vp, vp, i, ctypes.c_longlong, i, i, vp, vp, vp]
         L.sdp_merge.restype = i
+        L.sdp_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp]
+        L.sdp_fwd_varlen.restype = i
         L.sdp_fwd_splitkv_count.argtypes = [i, i, i, i, i, i, i, i]
         L.sdp_fwd_splitkv_count.restype = i
         L.sdp_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
@@ -200,6 +203,67 @@ def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
         rc = sdp_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                          0 if lse is None else lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
                          _DTYPE_CODE[q.dtype], _stream_handle(stream, q.device), causal=causal)
+    _check(rc)
+    return out, lse
+
+
+def sdp_fwd_varlen_ptr(q: int, k: int, v: int, o: int, lse: int, cu_q: int, cu_k: int, nseq: int, Hq: int,
+                       Hkv: int, total_q: int, total_k: int, max_seqlen_q: int, D: int, scale: float, dtype: int,
+                       causal: bool = False, stream: int = 0) -> int:
+    """The raw C call sdp_fwd_varlen with integer addresses; returns the status code."""
+    return int(lib().sdp_fwd_varlen(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.c_void_p(o),
+                                    ctypes.c_void_p(lse), ctypes.c_void_p(cu_q), ctypes.c_void_p(cu_k), int(nseq),
+                                    int(Hq), int(Hkv), int(total_q), int(total_k), int(max_seqlen_q), int(D),
+                                    ctypes.c_float(scale), int(dtype), int(bool(causal)), ctypes.c_void_p(stream)))
+
+
+def sdp_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                   cu_seqlens_k: torch.Tensor, max_seqlen_q: int, scale: float | None = None,
+                   causal: bool = False, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                   return_lse: bool = True, stream=None):
+    """Attention over a variable-length batch packed back to back.
+
+    q: [total_q, Hq, D]; k, v: [total_k, Hkv, D] (token, head, dim), fp16 or
+    bf16, contiguous, on one CUDA device; cu_seqlens_q / cu_seqlens_k: int32
+    [nseq + 1] offsets on that device; max_seqlen_q: a host int >= every query
+    length. Returns (o like q, lse fp32 [Hq, total_q] or None). Sequence
+    offsets are checked on the device: bad ones show up in poll_status() as
+    SDP_ERR_BAD_SEQLENS.
+    """
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be 3-D [tokens, heads, D]")
+    tensors = (q, k, v, cu_seqlens_q, cu_seqlens_k)
+    if not all(t.is_cuda for t in tensors) or len({t.device for t in tensors}) != 1:
+        raise ValueError("q, k, v and the offsets must be CUDA tensors on one device")
+    if q.dtype not in _DTYPE_CODE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, float16 or bfloat16")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise ValueError("sequence offsets must be int32")
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape != cu_seqlens_k.shape or cu_seqlens_q.numel() < 2:
+        raise ValueError("sequence offsets must be 1-D [nseq + 1] of equal length")
+    if not all(t.is_contiguous() for t in tensors):
+        raise ValueError("q, k, v and the offsets must be contiguous")
+    total_q, Hq, D = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    if k.shape[2] != D or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != q.device:
+        raise ValueError("out must be a contiguous tensor shaped and typed like q")
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.shape != (Hq, total_q) or lse.dtype != torch.float32 or not lse.is_contiguous()
+                            or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 tensor [Hq, total_q] on q's device")
+    with torch.cuda.device(q.device):
+        rc = sdp_fwd_varlen_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                0 if lse is None else lse.data_ptr(), cu_seqlens_q.data_ptr(),
+                                cu_seqlens_k.data_ptr(), cu_seqlens_q.numel() - 1, Hq, Hkv, total_q, total_k,
+                                int(max_seqlen_q), D, float(scale), _DTYPE_CODE[q.dtype], causal,
+                                _stream_handle(stream, q.device))
     _check(rc)
     return out, lse
 

@@ -105,6 +105,28 @@ int encode_map(CUtensorMap *map, const void *base, int dtype, int D, long long r
     return SDP_OK;
 }
 
+// 3-D map over a (token, head, dim) 16-bit tensor [rows, heads, D], in the
+// same (column, row, plane) coordinate order as encode_map: plane = head, with
+// a row stride of heads * D elements and a plane stride of D.
+int encode_map_thd(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long heads)
+{
+    EncodeTiledFn enc = encoder();
+    if (enc == nullptr)
+        return cuda_fail(cudaErrorNotSupported);
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(heads)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * D * 2, static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = enc(map, dtype == SDP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return cuda_fail(cudaErrorInvalidValue);
+    return SDP_OK;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
@@ -301,6 +323,81 @@ int sdp_fwd_causal(const void *q, const void *k, const void *v, void *o, float *
     return forward(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, dtype, 1, stream);
 }
 
+int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu_seqlens_q,
+                   const int *cu_seqlens_k, int nseq, int Hq, int Hkv, int total_q, int total_k, int max_seqlen_q,
+                   int D, float scale, int dtype, int causal, void *stream)
+{
+    if (dtype != SDP_FP16 && dtype != SDP_BF16)
+        return SDP_ERR_UNSUPPORTED;
+    if (D != 128 && D != 256)
+        return SDP_ERR_UNSUPPORTED;
+    if (nseq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0)
+        return SDP_ERR_INVALID_ARG;
+    if (total_q == 0)
+        return SDP_OK;  // no query rows (empty tensors may have null pointers): nothing to compute
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || cu_seqlens_q == nullptr ||
+        cu_seqlens_k == nullptr || max_seqlen_q == 0)
+        return SDP_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || o == q || o == k || o == v)
+        return SDP_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+        return SDP_ERR_ALIGNMENT;
+    const long long n_qtiles = (static_cast<long long>(max_seqlen_q) + 127) / 128;
+    const long long n_kvtiles = (static_cast<long long>(total_k) + 127) / 128;
+    const long long units = static_cast<long long>(nseq) * Hq * n_qtiles;
+    if (units > INT32_MAX)
+        return SDP_ERR_OVERFLOW;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    unsigned int *status = nullptr;
+    int rc = device_state(dev, &status);
+    if (rc != SDP_OK)
+        return rc;
+    // A batch without keys still gets valid maps (one row); no load is issued then.
+    const long long kv_rows = total_k > 0 ? total_k : 1;
+    sdp::LaunchMaps maps;
+    if ((rc = encode_map_thd(&maps.q, q, dtype, D, total_q, Hq)) != SDP_OK ||
+        (rc = encode_map_thd(&maps.k, k, dtype, D, kv_rows, Hkv)) != SDP_OK ||
+        (rc = encode_map_thd(&maps.v, v, dtype, D, kv_rows, Hkv)) != SDP_OK ||
+        (rc = encode_map_thd(&maps.o, o, dtype, D, total_q, Hq)) != SDP_OK)
+        return rc;
+    maps.k_half = maps.k;  // unused: variable-length batches run the single-CTA kernel
+
+    sdp::KernelParams p{};
+    p.lse = lse;
+    p.status = status;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.Sq = total_q;
+    p.Skv = total_k;
+    p.n_qtiles = static_cast<int>(n_qtiles);
+    p.n_kvtiles = static_cast<int>(n_kvtiles);
+    p.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);  // scale * log2(e)
+    p.timeout_ns = static_cast<unsigned long long>(g_timeout_ms.load()) * 1000000ull;
+    p.debug_flags = g_debug_flags.load();
+    p.causal = causal ? 1 : 0;
+    p.kv_splits = 1;
+    p.tiles_per_split = static_cast<int>(n_kvtiles > 0 ? n_kvtiles : 1);
+    p.planes_q = Hq;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.o = o;
+    p.o_row_stride = static_cast<long long>(Hq) * D;
+
+    const int grid = static_cast<int>(units);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (D == 128)
+        e = dtype == SDP_BF16 ? sdp::launch_d128_bf16(maps, p, grid, st) : sdp::launch_d128_fp16(maps, p, grid, st);
+    else
+        e = dtype == SDP_BF16 ? sdp::launch_d256_bf16(maps, p, grid, st) : sdp::launch_d256_fp16(maps, p, grid, st);
+    return e == cudaSuccess ? SDP_OK : cuda_fail(e);
+}
+
 long long sdp_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int D, int dtype, int n_splits)
 {
     Shape sh;
@@ -382,7 +479,7 @@ int sdp_poll_status(void *stream)
         return cuda_fail(e);
     if ((e = cudaDeviceSynchronize()) != cudaSuccess)
         return cuda_fail(e);
-    return SDP_ERR_DEVICE_TIMEOUT;
+    return (word & 0xffu) == 7u ? SDP_ERR_BAD_SEQLENS : SDP_ERR_DEVICE_TIMEOUT;
 }
 
 unsigned int sdp_last_status_detail(void) { return g_last_detail.load(); }
@@ -411,12 +508,15 @@ const char *sdp_strerror(int code)
         return "CUDA call failed (see sdp_last_cuda_error)";
     case SDP_ERR_DEVICE_TIMEOUT:
         return "a kernel wait timed out; its output tile was not written";
+    case SDP_ERR_BAD_SEQLENS:
+        return "variable-length batch: sequence offsets out of range, decreasing, or longer than max_seqlen_q; "
+               "those sequences were not written";
     default:
         return "unknown status code";
     }
 }
 
-int sdp_version(void) { return 103; }
+int sdp_version(void) { return 104; }
 
 void sdp_shutdown(void)
 {

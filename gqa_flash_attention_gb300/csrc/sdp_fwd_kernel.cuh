@@ -47,6 +47,7 @@ enum : uint32_t {
     SITE_S_FULL = 4,
     SITE_P_FULL = 5,
     SITE_O_DONE = 6,
+    SITE_SEQLENS = 7,  // variable-length batch: sequence offsets out of range or not increasing
 };
 
 constexpr int DEBUG_NO_LOADS = 1;
@@ -161,6 +162,25 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// Geometry of one unit's sequence: where its Q/O rows and K/V rows start in
+// the (token) row coordinate, and how many of each it has. Without a
+// variable-length batch it is the whole plane.
+struct SeqGeom {
+    int q_row0, kv_row0, sq, skv;
+    bool ok;
+};
+
+__device__ __forceinline__ SeqGeom seq_geom(const KernelParams &p, int b)
+{
+    if (p.cu_q == nullptr)
+        return SeqGeom{0, 0, p.Sq, p.Skv, true};
+    const int q0 = __ldg(p.cu_q + b), q1 = __ldg(p.cu_q + b + 1);
+    const int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
+    const bool ok = 0 <= q0 && q0 <= q1 && q1 <= p.Sq && 0 <= k0 && k0 <= k1 && k1 <= p.Skv &&
+                    q1 - q0 <= p.n_qtiles * 128;
+    return SeqGeom{q0, k0, q1 - q0, k1 - k0, ok};
+}
+
 // Position of a chunk in the load order K_0, then for j = 0..n-1: K_{j+1} (if
 // any), V_j. Tiles are CPT chunks long; the producer and both issuers derive
 // ring slot = pos % NSLOTS and phase = (pos / NSLOTS) & 1 from it. Every
@@ -225,13 +245,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int bg = u / p.n_qtiles;  // b * Hkv + g
     const int b = bg / p.Hkv;
     const int g = bg - b * p.Hkv;
-    const int z_q = b * p.Hq + g * p.G + hi;  // (b, h) plane of Q, O and LSE
-    const int z_kv = bg;                      // (b, g) plane of K and V
-    const int q0 = qt * L::BM;
+    const bool varlen = p.cu_q != nullptr;
+    // (b, h) plane of Q, O and LSE and (b, g) plane of K and V; heads h and g
+    // in a variable-length batch, whose sequences are runs of rows.
+    const int z_q = varlen ? g * p.G + hi : b * p.Hq + g * p.G + hi;
+    const int z_kv = varlen ? g : bg;
+    const int q0 = qt * L::BM;  // first query row of the unit within its sequence
+    const SeqGeom sg = seq_geom(p, b);
+    if (!sg.ok) {
+        if (threadIdx.x == 0) {
+            const uint32_t cta = blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu;
+            atomicCAS(p.status, 0u, SITE_SEQLENS | (cta << 8));
+        }
+        return;
+    }
+    if (q0 >= sg.sq)
+        return;  // a tile past the end of a shorter sequence: nothing to do
+    const int n_kv = (sg.skv + L::BN - 1) / L::BN;
     // Tiles this unit reads: all of them, or (causal) those holding keys <= its last row.
     const int t0 = split * p.tiles_per_split;  // first KV tile of this unit
-    const int n = p.causal ? min(p.n_kvtiles, qt + 1) : min(p.n_kvtiles - t0, p.tiles_per_split);
+    const int n = p.causal ? min(n_kv, qt + 1) : min(n_kv - t0, p.tiles_per_split);
     const int z_out = split * p.planes_q + z_q;  // output plane of O and LSE
+    const int q_row = sg.q_row0 + q0;            // row coordinate of the tile in Q and O
+    if (n <= 0) {
+        // A sequence without keys: its rows attend to nothing, O = 0 and LSE = -inf.
+        const int rows = min(L::BM, sg.sq - q0);
+        for (int i = threadIdx.x; i < rows * (D / 8); i += NUM_THREADS) {
+            const int r = i / (D / 8), c8 = i % (D / 8);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) +
+                                                   static_cast<size_t>(q_row + r) * p.o_row_stride +
+                                                   static_cast<size_t>(z_q) * D) + c8;
+            *dst = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (p.lse != nullptr)
+            for (int r = threadIdx.x; r < rows; r += NUM_THREADS)
+                p.lse[static_cast<size_t>(z_out) * p.Sq + q_row + r] = -INFINITY;
+        return;
+    }
+    // A variable-length tile that ends past its sequence is stored row by row.
+    const bool direct_store = varlen && q0 + L::BM > sg.sq;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
@@ -276,7 +328,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::mbar_arrive_expect_tx_w(q_full, L::Q_BYTES);
 #pragma unroll
                 for (int c = 0; c < D / L::BOX_COLS; ++c)
-                    ptx::tma_load_3d_w(s_q + c * L::BOX_BYTES, &tm_q, q_full, c * L::BOX_COLS, q0, z_q);
+                    ptx::tma_load_3d_w(s_q + c * L::BOX_BYTES, &tm_q, q_full, c * L::BOX_COLS, q_row, z_q);
                 q_armed = true;
                 auto load_tile = [&](const CUtensorMap *map, int j) -> bool {
 #pragma unroll
@@ -287,8 +339,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             return false;
                         ptx::mbar_arrive_expect_tx_w(full, L::CHUNK_BYTES);
                         const uint32_t dst = s_ring + slot * L::CHUNK_BYTES;
-                        ptx::tma_load_3d_w(dst, map, full, ch * 128, (t0 + j) * L::BN, z_kv);
-                        ptx::tma_load_3d_w(dst + L::BOX_BYTES, map, full, ch * 128 + L::BOX_COLS, (t0 + j) * L::BN, z_kv);
+                        const int y = sg.kv_row0 + (t0 + j) * L::BN;
+                        ptx::tma_load_3d_w(dst, map, full, ch * 128, y, z_kv);
+                        ptx::tma_load_3d_w(dst + L::BOX_BYTES, map, full, ch * 128 + L::BOX_COLS, y, z_kv);
                         armed_mask |= 1u << slot;
                         armed_par = (armed_par & ~(1u << slot)) | (ph << slot);
                         if (++slot == NS) {
@@ -422,7 +475,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 s[i] = __uint_as_float(sr[i]);
 
             // keys of this tile the row sees (>= 1): all < Skv, and (causal) <= the row itself
-            const int valid = (p.causal ? min(p.Skv, q0 + row + 1) : p.Skv) - (t0 + j) * L::BN;  // >= 1
+            const int valid = (p.causal ? min(sg.skv, q0 + row + 1) : sg.skv) - (t0 + j) * L::BN;  // >= 1
             if (valid < L::BN) {
 #pragma unroll
                 for (int i = 1; i < 128; ++i)
@@ -529,6 +582,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                if (direct_store) {
+                    // the rows of this sequence only, 64 bytes per row per step
+                    if (q0 + row < sg.sq) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) +
+                                                               static_cast<size_t>(q_row + row) * p.o_row_stride +
+                                                               static_cast<size_t>(z_q) * D + 32 * cc);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                    continue;
+                }
                 // 32 columns = four 16-byte units of row `row` in box cc/2, 128-byte swizzled.
                 const uint32_t row_addr = s_q + (cc >> 1) * L::BOX_BYTES + row * 128;
 #pragma unroll
@@ -538,15 +603,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                  pk[4 * v + 2], pk[4 * v + 3]);
                 }
             }
-            if (p.lse != nullptr && q0 + row < p.Sq)
-                p.lse[static_cast<size_t>(z_out) * p.Sq + q0 + row] = (m_used + ptx::lg2(l)) * LN2;
+            if (p.lse != nullptr && q0 + row < sg.sq)
+                p.lse[static_cast<size_t>(z_out) * p.Sq + q_row + row] = (m_used + ptx::lg2(l)) * LN2;
             ptx::fence_proxy_async_smem();
         }
         ptx::named_bar_sync(1, 128);
-        if (threadIdx.x == 0 && !*abort_flag) {
+        if (threadIdx.x == 0 && !*abort_flag && !direct_store) {
 #pragma unroll
             for (int c2 = 0; c2 < D / L::BOX_COLS; ++c2)
-                ptx::tma_store_3d(&tm_o, s_q + c2 * L::BOX_BYTES, c2 * L::BOX_COLS, q0, z_out);
+                ptx::tma_store_3d(&tm_o, s_q + c2 * L::BOX_BYTES, c2 * L::BOX_COLS, q_row, z_out);
             ptx::bulk_commit_group();
             ptx::bulk_wait_group_all();
         }

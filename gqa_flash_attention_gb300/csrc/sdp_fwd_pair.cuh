@@ -491,7 +491,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 // with the head-in-group index fastest that holds when G is even.
 inline bool use_pair(const KernelParams &p, int grid)
 {
-    if (p.debug_flags & DEBUG_SINGLE_CTA)
+    if ((p.debug_flags & DEBUG_SINGLE_CTA) || p.cu_q != nullptr)  // variable-length batches: single-CTA kernel
         return false;
     if (p.causal && (p.G % 2) != 0)
         return false;

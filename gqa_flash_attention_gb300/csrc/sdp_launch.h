@@ -21,6 +21,15 @@ struct KernelParams {
     // reading KV tiles [s * tiles_per_split, +tiles_per_split) and writing its
     // partial O / LSE to output plane s * planes_q + (b, h). 1 / n_kvtiles otherwise.
     int kv_splits, tiles_per_split, planes_q;
+    // Variable-length batches (cu_q != nullptr): sequence b owns Q/O rows
+    // [cu_q[b], cu_q[b+1]) and K/V rows [cu_k[b], cu_k[b+1]) of tensors laid out
+    // (token, head, dim); the planes are heads, Sq / Skv hold the token totals,
+    // LSE is [Hq, total_q], and n_qtiles covers the longest sequence. A tile
+    // that ends past its sequence is written row by row through `o`, element
+    // (token t, head h) at o + t * o_row_stride + h * D.
+    const int *cu_q, *cu_k;
+    void *o;
+    long long o_row_stride;
 };
 
 // Tensor maps of one launch: Q, K, V, O with 128-row boxes, and K with 64-row

@@ -38,6 +38,7 @@ extern "C" {
 #define SDP_ERR_OVERFLOW (-4)       /* index space does not fit the kernel's 32-bit tile and coordinate counters */
 #define SDP_ERR_CUDA (-5)           /* a CUDA runtime/driver call failed; sdp_last_cuda_error() gives the code */
 #define SDP_ERR_DEVICE_TIMEOUT (-6) /* a kernel gave up on a bounded wait and flagged its status word */
+#define SDP_ERR_BAD_SEQLENS (-7)    /* sdp_fwd_varlen: a kernel found bad sequence offsets (status word) */
 
 /*
  * sdp_fwd — O = softmax(Q K^T * scale) V and LSE, enqueued on `stream`.
@@ -141,6 +142,39 @@ int sdp_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float 
                     int n_splits, void *workspace, unsigned long long workspace_bytes, void *stream);
 
 /*
+ * sdp_fwd_varlen — attention over a batch of sequences of different lengths
+ * packed back to back (no counterpart on the pages: the plain generalisation
+ * of a ragged last tile to a batch of ragged sequences). Sequence b owns
+ * query rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key rows
+ * [cu_seqlens_k[b], cu_seqlens_k[b+1]); each query row attends to its own
+ * sequence's keys only, as in sdp_fwd (causal != 0: row i of a sequence sees
+ * that sequence's keys 0..i, top-left). A row of a sequence with no keys gets
+ * O = 0 and LSE = -inf.
+ *
+ * q       device, [total_q, Hq, D] (token, head, dim), contiguous, dtype
+ * k, v    device, [total_k, Hkv, D], contiguous, dtype
+ * o       device, [total_q, Hq, D] (written); lse [Hq, total_q] fp32 or NULL
+ * cu_seqlens_q, cu_seqlens_k  device int32 [nseq + 1]: 0, then non-decreasing
+ *         offsets, ending at total_q / total_k
+ * max_seqlen_q  host int >= every query length (it sizes the grid: 128-row
+ *         tiles of the longest sequence per (sequence, head))
+ * Hq % Hkv == 0, D in {128, 256}; total_q == 0 returns SDP_OK at once (null
+ * pointers allowed then), before the other checks.
+ *
+ * Ownership and aliasing as sdp_fwd. The offsets live on the device, so they
+ * are checked by the kernel: a sequence whose offsets leave [0, total], go
+ * down, or give more rows than max_seqlen_q rounded up to a multiple of 128
+ * is not computed, and the next sdp_poll_status returns SDP_ERR_BAD_SEQLENS. Inputs must be finite: the key rows after a
+ * sequence's last key in its last 128-key tile belong to the next sequence
+ * and are read, with weight exactly 0. Every tile runs on the single-CTA
+ * kernel; tiles that end past their sequence store O row by row.
+ */
+int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                   const int *cu_seqlens_q, const int *cu_seqlens_k, int nseq, int Hq, int Hkv,
+                   int total_q, int total_k, int max_seqlen_q, int D, float scale, int dtype, int causal,
+                   void *stream);
+
+/*
  * sdp_fwd_noalloc — sdp_fwd for callers that cannot allocate device memory.
  * The paper has no counterpart: this is a library-usage variant, not a step of
  * the method.
@@ -180,7 +214,8 @@ int sdp_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float 
  * sdp_poll_status — synchronise `stream`, then read and clear the current
  * device's status word. Returns SDP_OK, SDP_ERR_DEVICE_TIMEOUT (a kernel
  * abandoned a wait after the timeout and returned without writing its
- * tile), or SDP_ERR_CUDA (the synchronisation itself failed).
+ * tile), SDP_ERR_BAD_SEQLENS (sdp_fwd_varlen found bad offsets), or
+ * SDP_ERR_CUDA (the synchronisation itself failed).
  */
 int sdp_poll_status(void *stream);
 
@@ -188,7 +223,7 @@ int sdp_poll_status(void *stream);
  * sdp_last_status_detail — the raw status word read by the last
  * sdp_poll_status() that found an error: bits 0-7 name the wait that timed
  * out (1 Q load, 2 KV slot empty, 3 KV slot full, 4 S ready, 5 P ready,
- * 6 O done), bits 8-31 the CTA index (saturating).
+ * 6 O done) or 7 for bad sequence offsets, bits 8-31 the CTA index (saturating).
  */
 unsigned int sdp_last_status_detail(void);
 
@@ -215,7 +250,7 @@ int sdp_last_cuda_error(void);
 /* A static, human-readable description of a status code. */
 const char *sdp_strerror(int code);
 
-/* ABI version: 100 * major + minor (101: sdp_fwd_causal; 102: sdp_merge; 103: split-KV). */
+/* ABI version: 100 * major + minor (101: sdp_fwd_causal; 102: sdp_merge; 103: split-KV; 104: varlen). */
 int sdp_version(void);
 
 /* Free the per-device status words. Call only with no sdp work in flight. */

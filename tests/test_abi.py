@@ -37,8 +37,8 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_version_and_messages(L):
-    assert L.sdp_version() == 103
-    for code in range(-6, 1):
+    assert L.sdp_version() == 104
+    for code in range(-7, 1):
         assert len(sdp.strerror(code)) > 0
     assert sdp.strerror(-99) == "unknown status code"
 
@@ -126,3 +126,32 @@ def test_split_kv_validation_errors_launch_nothing(L, kw, code):
 def test_split_kv_planning_rejects_bad_sizes(L, args, code):
     assert L.sdp_fwd_splitkv_count(*args) == code
     assert L.sdp_fwd_splitkv_workspace_bytes(*args) == code
+
+
+def varlen_call(**kw):
+    args = dict(q=A, k=2 * A, v=3 * A, o=4 * A, lse=5 * A, cu_q=6 * A, cu_k=7 * A, nseq=2, Hq=4, Hkv=2,
+                total_q=300, total_k=300, max_seqlen_q=200, D=128, scale=0.088, dtype=sdp.SDP_FP16)
+    args.update(kw)
+    return sdp.sdp_fwd_varlen_ptr(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=64), sdp.SDP_ERR_UNSUPPORTED),
+    (dict(dtype=2), sdp.SDP_ERR_UNSUPPORTED),
+    (dict(cu_q=0), sdp.SDP_ERR_INVALID_ARG),
+    (dict(cu_k=0), sdp.SDP_ERR_INVALID_ARG),
+    (dict(max_seqlen_q=0), sdp.SDP_ERR_INVALID_ARG),
+    (dict(nseq=0), sdp.SDP_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), sdp.SDP_ERR_INVALID_ARG),
+    (dict(total_k=-1), sdp.SDP_ERR_INVALID_ARG),
+    (dict(max_seqlen_q=-1), sdp.SDP_ERR_INVALID_ARG),
+    (dict(o=2 * A), sdp.SDP_ERR_INVALID_ARG),
+    (dict(scale=math.inf), sdp.SDP_ERR_INVALID_ARG),
+    (dict(cu_q=6 * A + 2), sdp.SDP_ERR_ALIGNMENT),
+    (dict(q=A + 4), sdp.SDP_ERR_ALIGNMENT),
+    (dict(total_q=0), sdp.SDP_OK),
+    (dict(total_q=0, q=0, o=0), sdp.SDP_OK),
+    (dict(nseq=1 << 20, Hq=1 << 12, Hkv=1, max_seqlen_q=1 << 10), sdp.SDP_ERR_OVERFLOW),
+])
+def test_varlen_validation_errors_launch_nothing(L, kw, code):
+    assert varlen_call(**kw) == code
