@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 from gqa_flash_attention_gb300 import workloads  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense fp16/bf16 tensor peak"
+BENCH_WORKLOADS = {**workloads.ALL_WORKLOADS, **workloads.VARLEN_WORKLOADS}
 FALLBACK_PEAK_TFLOPS = 1900.0
 
 
@@ -44,7 +45,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.ALL_WORKLOADS))
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(BENCH_WORKLOADS))
     ap.add_argument("--cpu-rows", type=int, default=0, help="query rows per head in the CPU sample (0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -171,26 +172,60 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None, "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def is_varlen(w):
+    return isinstance(w, workloads.VarlenWorkload)
+
+
 def cpu_rows_auto(w):
     # about 10-20 s of oracle work on a 16-core host (the oracle runs near 60 fp64 GFLOP/s there)
-    per_row = 4.0 * w.Skv * w.D
     target = 8e11
+    if is_varlen(w):
+        per_row = 4.0 * w.D * w.Hq * sum(w.lens_k)  # one row per sequence and head
+        return int(max(2, min(w.max_q, target / per_row)))
+    per_row = 4.0 * w.Skv * w.D
     return int(max(2, min(w.Sq, target / (per_row * w.B * w.Hq))))
 
 
+def host_inputs(w):
+    return workloads.make_varlen_inputs(w) if is_varlen(w) else workloads.make_inputs(w)
+
+
 def run_cpu_oracle(w, rows_per_head, q=None, k=None, v=None):
-    """Time the oracle on a sample of query rows; returns (tflops, seconds, rows, threads)."""
+    """Time the oracle on a sample of query rows; returns (tflops, seconds, sample description, threads)."""
     import oracle
     if q is None:
-        q, k, v = workloads.make_inputs(w)
-    rows = workloads.sample_rows(w, rows_per_head, seed=1234)
+        q, k, v = host_inputs(w)
     dt = oracle.FP16 if w.dtype == "fp16" else oracle.BF16
+    if is_varlen(w):
+        # rows_per_head rows of every (sequence, head), each sequence on its own through the dense oracle
+        rng = np.random.default_rng(1234)
+        sec, seen = 0.0, 0
+        for b in range(w.nseq):
+            lq, lk = w.lens_q[b], w.lens_k[b]
+            if lq == 0 or lk == 0:
+                continue
+            m = min(rows_per_head, lq)
+            rows = np.sort(np.stack([rng.choice(lq, size=m, replace=False) for _ in range(w.Hq)]))
+            rows = rows.reshape(1, w.Hq, m).astype(np.int32)
+            qs = q[w.cu_q[b]:w.cu_q[b + 1]].permute(1, 0, 2).unsqueeze(0).contiguous()
+            ks = k[w.cu_k[b]:w.cu_k[b + 1]].permute(1, 0, 2).unsqueeze(0).contiguous()
+            vs = v[w.cu_k[b]:w.cu_k[b + 1]].permute(1, 0, 2).unsqueeze(0).contiguous()
+            t0 = time.perf_counter()
+            oracle.sdp_fwd_rows(qs, ks, vs, dt, (1, w.Hq, w.Hkv, lq, lk, w.D), w.softmax_scale, rows,
+                                causal=w.causal)
+            sec += time.perf_counter() - t0
+            seen += int((np.minimum(rows.astype(np.int64) + 1, lk) if w.causal else np.full(rows.shape, lk)).sum())
+        desc = (f"{rows_per_head} query rows per (sequence, head) x {w.nseq} sequences x {w.Hq} heads of "
+                f"{w.name}, all of each sequence's keys")
+        return 4.0 * seen * w.D / sec / 1e12, sec, desc, oracle.num_threads()
+    rows = workloads.sample_rows(w, rows_per_head, seed=1234)
     t0 = time.perf_counter()
     oracle.sdp_fwd_rows(q, k, v, dt, w.shape, w.softmax_scale, rows, causal=w.causal)
     sec = time.perf_counter() - t0
     seen = (np.minimum(rows.astype(np.int64) + 1, w.Skv) if w.causal else np.full(rows.shape, w.Skv)).sum()
     flops = 4.0 * float(seen) * w.D
-    return flops / sec / 1e12, sec, rows.shape[2], oracle.num_threads()
+    desc = f"{rows.shape[2]} query rows per (batch, head) x {w.B * w.Hq} heads of {w.name}, all {w.Skv} keys"
+    return flops / sec / 1e12, sec, desc, oracle.num_threads()
 
 
 # ------------------------------------------------------------------ arms
@@ -202,17 +237,16 @@ def reference_arm(args, w):
     import oracle
     oracle.build()
     rows = args.cpu_rows or max(2, cpu_rows_auto(w) // 4)
-    q, k, v = workloads.make_inputs(w)
+    q, k, v = host_inputs(w)
     for _ in range(args.warmup):
         run_cpu_oracle(w, max(2, rows // 8), q, k, v)
     vals, secs = [], []
     for _ in range(args.steps):
-        tf, sec, nrows, threads = run_cpu_oracle(w, rows, q, k, v)
+        tf, sec, desc, threads = run_cpu_oracle(w, rows, q, k, v)
         vals.append(tf)
         secs.append(sec)
     value = statistics.median(vals)
-    sample = (f"{nrows} query rows per (batch, head) x {w.B * w.Hq} heads of {w.name}, all {w.Skv} keys, "
-              f"per step")
+    sample = desc + ", per step"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.median(secs),
@@ -237,7 +271,10 @@ def launch_shape(w):
 def kernel_name(w):
     """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
     the units of each (batch, KV head) pair up (and, causal, share the query
-    tile), else the single-CTA kernel; split-KV adds the merge kernel."""
+    tile), else the single-CTA kernel; split-KV adds the merge kernel;
+    variable-length batches run the single-CTA kernel."""
+    if is_varlen(w):
+        return "sdp_fwd_kernel"
     sq, G = launch_shape(w)
     n_qtiles = (sq + 127) // 128
     pair = (n_qtiles * G) % 2 == 0 and not (w.causal and G % 2)
@@ -253,6 +290,14 @@ def needs_flush(w):
 
 
 def config_of(w, n):
+    if is_varlen(w):
+        return {"workload": w.name, "nseq": w.nseq, "lens_q": list(w.lens_q), "lens_k": list(w.lens_k),
+                "total_q": w.total_q, "total_k": w.total_k, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                "io_dtype": w.dtype, "scale": w.softmax_scale, "causal": w.causal, "layout": "tokens, heads, D",
+                "flops_per_step_per_gpu": w.flops(),
+                "l2": ("L2 flushed (256 MB write) before every timed step; only the call is timed" if needs_flush(w)
+                       else "inputs larger than L2; no flush"),
+                "parallelism": "replicas" if n > 1 else "single GPU"}
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv, "D": w.D,
             "io_dtype": w.dtype, "scale": w.softmax_scale, "causal": w.causal, "peaky_k": w.peaky_k,
             "flops_per_step_per_gpu": w.flops(), "kv_splits": w.kv_splits,
@@ -272,15 +317,23 @@ def ours_arm(args, w):
     torch.cuda.set_device(dev)
     sdp.lib()
 
-    q_h, k_h, v_h = workloads.make_inputs(w)
+    q_h, k_h, v_h = host_inputs(w)
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     o = torch.empty_like(q)
-    lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
+    if is_varlen(w):
+        lse = torch.empty(w.Hq, w.total_q, dtype=torch.float32, device=dev)
+        cu_h = [torch.from_numpy(w.cu_q), torch.from_numpy(w.cu_k)]
+        cu_q, cu_k = (t.to(dev) for t in cu_h)
+    else:
+        lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
+        cu_h = []
     stream = torch.cuda.current_stream(dev)
 
     launches_per_step = 1
     ws = None
-    if w.kv_splits != 1:
+    if is_varlen(w):
+        pass
+    elif w.kv_splits != 1:
         dt = sdp.SDP_BF16 if w.dtype == "bf16" else sdp.SDP_FP16
         splits = sdp.splitkv_count(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, dt, w.kv_splits)
         need = sdp.splitkv_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, dt, w.kv_splits)
@@ -288,8 +341,12 @@ def ours_arm(args, w):
         launches_per_step = 2 if splits > 1 else 1
 
     def call():
-        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse, causal=w.causal, kv_splits=w.kv_splits,
-                    workspace=ws)
+        if is_varlen(w):
+            sdp.sdp_fwd_varlen(q, k, v, cu_q, cu_k, w.max_q, scale=w.softmax_scale, causal=w.causal, out=o,
+                               lse=lse)
+        else:
+            sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse, causal=w.causal, kv_splits=w.kv_splits,
+                        workspace=ws)
 
     flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev) if needs_flush(w) else None
     for _ in range(args.warmup):
@@ -297,7 +354,7 @@ def ours_arm(args, w):
     torch.cuda.synchronize(dev)
     if sdp.poll_status() != sdp.SDP_OK:
         raise RuntimeError("kernel reported a timeout during warm-up")
-    use_graph = args.graph == "on" or (args.graph == "auto" and w.kv_splits != 1)
+    use_graph = args.graph == "on" or (args.graph == "auto" and not is_varlen(w) and w.kv_splits != 1)
     step = call
     if use_graph:
         graph = torch.cuda.CUDAGraph()
@@ -342,6 +399,7 @@ def ours_arm(args, w):
     e2e = None
     if not args.no_e2e:
         qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+        cu_p = [t.pin_memory() for t in cu_h]
         op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
         n_e2e = max(3, K // 10)
@@ -350,6 +408,9 @@ def ours_arm(args, w):
             q.copy_(qp, non_blocking=True)
             k.copy_(kp, non_blocking=True)
             v.copy_(vp, non_blocking=True)
+            if cu_p:
+                cu_q.copy_(cu_p[0], non_blocking=True)
+                cu_k.copy_(cu_p[1], non_blocking=True)
             call()
             op.copy_(o, non_blocking=True)
             lp.copy_(lse, non_blocking=True)
@@ -368,7 +429,7 @@ def ours_arm(args, w):
         te = torch.tensor([e0.elapsed_time(e1) / n_e2e], dtype=torch.float64, device=dev)
         if world > 1:
             torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-        h2d = sum(t_.numel() * t_.element_size() for t_ in (q_h, k_h, v_h))
+        h2d = sum(t_.numel() * t_.element_size() for t_ in (q_h, k_h, v_h, *cu_h))
         d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
         e2e = {"value": world * w.flops() / (float(te.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
@@ -400,10 +461,9 @@ def ours_arm(args, w):
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         rows = args.cpu_rows or cpu_rows_auto(w)
-        tf, sec, nrows, threads = run_cpu_oracle(w, rows, q_h, k_h, v_h)
+        tf, sec, desc, threads = run_cpu_oracle(w, rows, q_h, k_h, v_h)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{nrows} query rows per (batch, head) x {w.B * w.Hq} heads of {w.name}, all {w.Skv} "
-                         f"keys ({sec:.1f} s)"}
+               "sample": f"{desc} ({sec:.1f} s)"}
 
     cfg = config_of(w, world)
     cfg["cuda_graph"] = use_graph
@@ -461,7 +521,7 @@ def merge_arm(args, w):
 
 def main():
     args = parse()
-    w = workloads.ALL_WORKLOADS[args.workload]
+    w = BENCH_WORKLOADS[args.workload]
     if args.op == "merge":
         merge_arm(args, w)
     elif args.impl == "reference":
