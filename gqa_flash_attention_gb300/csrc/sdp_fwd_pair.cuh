@@ -338,52 +338,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     if (i >= valid)
                         s[i] = s[0];
             }
+            // Row extreme of the raw scores (maximum of s * c: of s when c >= 0, else
+            // its minimum), four three-input chains.
             float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
             if (c >= 0.f) {
 #pragma unroll
-                for (int i = 4; i < 128; i += 4) {
-                    mx0 = fmaxf(mx0, s[i]);
-                    mx1 = fmaxf(mx1, s[i + 1]);
-                    mx2 = fmaxf(mx2, s[i + 2]);
-                    mx3 = fmaxf(mx3, s[i + 3]);
+                for (int i = 4; i < 124; i += 8) {
+                    mx0 = ptx::max3(mx0, s[i], s[i + 1]);
+                    mx1 = ptx::max3(mx1, s[i + 2], s[i + 3]);
+                    mx2 = ptx::max3(mx2, s[i + 4], s[i + 5]);
+                    mx3 = ptx::max3(mx3, s[i + 6], s[i + 7]);
                 }
-                mx0 = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                mx0 = ptx::max3(mx0, s[124], s[125]);
+                mx1 = ptx::max3(mx1, s[126], s[127]);
+                mx0 = ptx::max3(mx0, mx1, fmaxf(mx2, mx3));
             } else {
 #pragma unroll
-                for (int i = 4; i < 128; i += 4) {
-                    mx0 = fminf(mx0, s[i]);
-                    mx1 = fminf(mx1, s[i + 1]);
-                    mx2 = fminf(mx2, s[i + 2]);
-                    mx3 = fminf(mx3, s[i + 3]);
+                for (int i = 4; i < 124; i += 8) {
+                    mx0 = ptx::min3(mx0, s[i], s[i + 1]);
+                    mx1 = ptx::min3(mx1, s[i + 2], s[i + 3]);
+                    mx2 = ptx::min3(mx2, s[i + 4], s[i + 5]);
+                    mx3 = ptx::min3(mx3, s[i + 6], s[i + 7]);
                 }
-                mx0 = fminf(fminf(mx0, mx1), fminf(mx2, mx3));
+                mx0 = ptx::min3(mx0, s[124], s[125]);
+                mx1 = ptx::min3(mx1, s[126], s[127]);
+                mx0 = ptx::min3(mx0, mx1, fminf(mx2, mx3));
             }
             const float m_tile = mx0 * c;
             const float m_new = (j == 0 || m_tile > m_used + RESCALE_THRESHOLD) ? m_tile : m_used;
             const float alpha = (j == 0 || m_new == m_used) ? 1.f : ptx::ex2(m_used - m_new);
             const float neg_m = -m_new;
 
+            // p = 2^(s * c - m), two elements per f32x2 instruction for the scaling
+            // and the running sums (each lane rounds exactly as fmaf / + would).
             uint32_t pk[64];
-            float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+            const uint64_t c2 = ptx::f2_pack(c, c), negm2 = ptx::f2_pack(neg_m, neg_m);
+            uint64_t sum01 = ptx::f2_pack(0.f, 0.f), sum23 = sum01;
 #pragma unroll
             for (int i = 0; i < 64; i += 2) {
-                float p0 = ptx::ex2(fmaf(s[2 * i], c, neg_m));
-                float p1 = ptx::ex2(fmaf(s[2 * i + 1], c, neg_m));
-                float p2 = ptx::ex2(fmaf(s[2 * i + 2], c, neg_m));
-                float p3 = ptx::ex2(fmaf(s[2 * i + 3], c, neg_m));
+                float x0, x1, x2, x3;
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i], s[2 * i + 1]), c2, negm2), x0, x1);
+                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i + 2], s[2 * i + 3]), c2, negm2), x2, x3);
+                float p0 = ptx::ex2(x0);
+                float p1 = ptx::ex2(x1);
+                float p2 = ptx::ex2(x2);
+                float p3 = ptx::ex2(x3);
                 if (valid < L::BN) {
                     p0 = (2 * i < valid) ? p0 : 0.f;
                     p1 = (2 * i + 1 < valid) ? p1 : 0.f;
                     p2 = (2 * i + 2 < valid) ? p2 : 0.f;
                     p3 = (2 * i + 3 < valid) ? p3 : 0.f;
                 }
-                sum0 += p0;
-                sum1 += p1;
-                sum2 += p2;
-                sum3 += p3;
+                sum01 = ptx::f2_add(sum01, ptx::f2_pack(p0, p1));
+                sum23 = ptx::f2_add(sum23, ptx::f2_pack(p2, p3));
                 pk[i] = pack2<BF16>(p0, p1);
                 pk[i + 1] = pack2<BF16>(p2, p3);
             }
+            float sum0, sum1, sum2, sum3;
+            ptx::f2_unpack(sum01, sum0, sum1);
+            ptx::f2_unpack(sum23, sum2, sum3);
             ptx::tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
             ptx::tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
             ptx::tmem_wait_st();
