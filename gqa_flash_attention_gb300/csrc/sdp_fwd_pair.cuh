@@ -332,11 +332,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
             // keys of this tile the row sees (>= 1): all < Skv, and (causal) <= the row itself
             const int valid = (p.causal ? min(p.Skv, q0 + row + 1) : p.Skv) - (t0 + j) * L::BN;
-            if (valid < L::BN) {
+            // Only a tile holding a key this row must not see (the ragged last tile,
+            // a causal diagonal) takes the masked path; the others run without any
+            // per-element test (a warp-uniform branch, not predication).
+            const bool tail = __any_sync(0xffffffffu, valid < L::BN);
+            if (tail) {
 #pragma unroll
                 for (int i = 1; i < 128; ++i)
                     if (i >= valid)
-                        s[i] = s[0];
+                        s[i] = s[0];  // neutral for the max; weights zeroed below
             }
             // Row extreme of the raw scores (maximum of s * c: of s when c >= 0, else
             // its minimum), four three-input chains.
@@ -374,26 +378,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             uint32_t pk[64];
             const uint64_t c2 = ptx::f2_pack(c, c), negm2 = ptx::f2_pack(neg_m, neg_m);
             uint64_t sum01 = ptx::f2_pack(0.f, 0.f), sum23 = sum01;
+            auto exp_tile = [&](auto masked) {
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-                float x0, x1, x2, x3;
-                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i], s[2 * i + 1]), c2, negm2), x0, x1);
-                ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i + 2], s[2 * i + 3]), c2, negm2), x2, x3);
-                float p0 = ptx::ex2(x0);
-                float p1 = ptx::ex2(x1);
-                float p2 = ptx::ex2(x2);
-                float p3 = ptx::ex2(x3);
-                if (valid < L::BN) {
-                    p0 = (2 * i < valid) ? p0 : 0.f;
-                    p1 = (2 * i + 1 < valid) ? p1 : 0.f;
-                    p2 = (2 * i + 2 < valid) ? p2 : 0.f;
-                    p3 = (2 * i + 3 < valid) ? p3 : 0.f;
+                for (int i = 0; i < 64; i += 2) {
+                    float x0, x1, x2, x3;
+                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i], s[2 * i + 1]), c2, negm2), x0, x1);
+                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i + 2], s[2 * i + 3]), c2, negm2), x2, x3);
+                    float p0 = ptx::ex2(x0);
+                    float p1 = ptx::ex2(x1);
+                    float p2 = ptx::ex2(x2);
+                    float p3 = ptx::ex2(x3);
+                    if constexpr (decltype(masked)::value) {
+                        p0 = (2 * i < valid) ? p0 : 0.f;
+                        p1 = (2 * i + 1 < valid) ? p1 : 0.f;
+                        p2 = (2 * i + 2 < valid) ? p2 : 0.f;
+                        p3 = (2 * i + 3 < valid) ? p3 : 0.f;
+                    }
+                    sum01 = ptx::f2_add(sum01, ptx::f2_pack(p0, p1));
+                    sum23 = ptx::f2_add(sum23, ptx::f2_pack(p2, p3));
+                    pk[i] = pack2<BF16>(p0, p1);
+                    pk[i + 1] = pack2<BF16>(p2, p3);
                 }
-                sum01 = ptx::f2_add(sum01, ptx::f2_pack(p0, p1));
-                sum23 = ptx::f2_add(sum23, ptx::f2_pack(p2, p3));
-                pk[i] = pack2<BF16>(p0, p1);
-                pk[i + 1] = pack2<BF16>(p2, p3);
-            }
+            };
+            if (tail)
+                exp_tile(std::true_type{});
+            else
+                exp_tile(std::false_type{});
             float sum0, sum1, sum2, sum3;
             ptx::f2_unpack(sum01, sum0, sum1);
             ptx::f2_unpack(sum23, sum2, sum3);
