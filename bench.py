@@ -272,9 +272,9 @@ def kernel_name(w):
     """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
     the units of each (batch, KV head) pair up (and, causal, share the query
     tile), else the single-CTA kernel; split-KV adds the merge kernel;
-    variable-length batches run the single-CTA kernel."""
+    variable-length batches pair up when the group size is even."""
     if is_varlen(w):
-        return "sdp_fwd_kernel"
+        return "sdp_fwd_pair_kernel" if (w.Hq // w.Hkv) % 2 == 0 else "sdp_fwd_kernel"
     sq, G = launch_shape(w)
     n_qtiles = (sq + 127) // 128
     pair = (n_qtiles * G) % 2 == 0 and not (w.causal and G % 2)

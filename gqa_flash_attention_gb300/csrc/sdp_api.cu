@@ -108,7 +108,8 @@ int encode_map(CUtensorMap *map, const void *base, int dtype, int D, long long r
 // 3-D map over a (token, head, dim) 16-bit tensor [rows, heads, D], in the
 // same (column, row, plane) coordinate order as encode_map: plane = head, with
 // a row stride of heads * D elements and a plane stride of D.
-int encode_map_thd(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long heads)
+int encode_map_thd(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long heads,
+                   unsigned box_rows = 128)
 {
     EncodeTiledFn enc = encoder();
     if (enc == nullptr)
@@ -116,7 +117,7 @@ int encode_map_thd(CUtensorMap *map, const void *base, int dtype, int D, long lo
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(heads)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * D * 2, static_cast<cuuint64_t>(D) * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estride[3] = {1, 1, 1};
     CUresult r = enc(map, dtype == SDP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                      const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -362,10 +363,10 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
     sdp::LaunchMaps maps;
     if ((rc = encode_map_thd(&maps.q, q, dtype, D, total_q, Hq)) != SDP_OK ||
         (rc = encode_map_thd(&maps.k, k, dtype, D, kv_rows, Hkv)) != SDP_OK ||
+        (rc = encode_map_thd(&maps.k_half, k, dtype, D, kv_rows, Hkv, 64)) != SDP_OK ||
         (rc = encode_map_thd(&maps.v, v, dtype, D, kv_rows, Hkv)) != SDP_OK ||
         (rc = encode_map_thd(&maps.o, o, dtype, D, total_q, Hq)) != SDP_OK)
         return rc;
-    maps.k_half = maps.k;  // unused: variable-length batches run the single-CTA kernel
 
     sdp::KernelParams p{};
     p.lse = lse;

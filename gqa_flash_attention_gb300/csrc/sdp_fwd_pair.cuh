@@ -138,13 +138,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int bg = u / p.n_qtiles;
     const int b = bg / p.Hkv;
     const int g = bg - b * p.Hkv;
-    const int z_q = b * p.Hq + g * p.G + hi;
-    const int z_kv = bg;
+    const bool varlen = p.cu_q != nullptr;
+    const int z_q = varlen ? g * p.G + hi : b * p.Hq + g * p.G + hi;
+    const int z_kv = varlen ? g : bg;
     const int q0 = qt * L::BM;
+    // Sequence geometry and the early exits are the same in both CTAs of a pair:
+    // a pair is two heads of one group on the same query tile of one sequence.
+    const SeqGeom sg = seq_geom(p, b);
+    if (!sg.ok) {
+        if (threadIdx.x == 0) {
+            const uint32_t cta = blockIdx.x < 0xFFFFFFu ? blockIdx.x : 0xFFFFFFu;
+            atomicCAS(p.status, 0u, SITE_SEQLENS | (cta << 8));
+        }
+        return;
+    }
+    if (q0 >= sg.sq)
+        return;
+    const int n_kv = (sg.skv + L::BN - 1) / L::BN;
     // Tiles this unit reads: all of them, or (causal) those holding keys <= its last row.
     const int t0 = split * p.tiles_per_split;  // first KV tile of this unit
-    const int n = p.causal ? min(p.n_kvtiles, qt + 1) : min(p.n_kvtiles - t0, p.tiles_per_split);
+    const int n = p.causal ? min(n_kv, qt + 1) : min(n_kv - t0, p.tiles_per_split);
     const int z_out = split * p.planes_q + z_q;  // output plane of O and LSE
+    const int q_row = sg.q_row0 + q0;            // row coordinate of the tile in Q and O
+    if (n <= 0) {
+        // A sequence without keys: its rows attend to nothing, O = 0 and LSE = -inf.
+        const int rows = min(L::BM, sg.sq - q0);
+        for (int i = threadIdx.x; i < rows * (D / 8); i += NUM_THREADS) {
+            const int r = i / (D / 8), c8 = i % (D / 8);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) +
+                                                   static_cast<size_t>(q_row + r) * p.o_row_stride +
+                                                   static_cast<size_t>(z_q) * D) + c8;
+            *dst = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (p.lse != nullptr)
+            for (int r = threadIdx.x; r < rows; r += NUM_THREADS)
+                p.lse[static_cast<size_t>(z_out) * p.Sq + q_row + r] = -INFINITY;
+        return;
+    }
+    // A variable-length tile that ends past its sequence is stored row by row.
+    const bool direct_store = varlen && q0 + L::BM > sg.sq;
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
@@ -188,7 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 ptx::mbar_arrive_expect_tx_w(q_full, 2 * L::Q_BYTES);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-                ptx::tma_load_3d_pair_w(s_q + c * L::Q_BOX_BYTES, &tm_q, q_full_l, c * 64, q0, z_q);
+                ptx::tma_load_3d_pair_w(s_q + c * L::Q_BOX_BYTES, &tm_q, q_full_l, c * 64, q_row, z_q);
             int slot = 0;
             uint32_t ph = 0;
             auto next_slot = [&](uint32_t &full_l, uint32_t &dst) -> bool {
@@ -212,7 +244,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
                     ptx::tma_load_3d_pair_w(dst + c * L::K_BOX_BYTES, &tm_k, full_l, c * 64,
-                                          (t0 + j) * L::BN + 64 * static_cast<int>(rank), z_kv);
+                                          sg.kv_row0 + (t0 + j) * L::BN + 64 * static_cast<int>(rank), z_kv);
                 return true;
             };
             auto load_v = [&](int j) -> bool {  // keys [j*128, +128), columns [rank*D/2, +D/2)
@@ -222,7 +254,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < D / 128; ++c)
                     ptx::tma_load_3d_pair_w(dst + c * L::V_BOX_BYTES, &tm_v, full_l,
-                                          static_cast<int>(rank) * (D / 2) + c * 64, (t0 + j) * L::BN, z_kv);
+                                          static_cast<int>(rank) * (D / 2) + c * 64, sg.kv_row0 + (t0 + j) * L::BN,
+                                          z_kv);
                 return true;
             };
             bool ok = load_k(0);
@@ -331,7 +364,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 s[i] = __uint_as_float(sr[i]);
 
             // keys of this tile the row sees (>= 1): all < Skv, and (causal) <= the row itself
-            const int valid = (p.causal ? min(p.Skv, q0 + row + 1) : p.Skv) - (t0 + j) * L::BN;
+            const int valid = (p.causal ? min(sg.skv, q0 + row + 1) : sg.skv) - (t0 + j) * L::BN;
             // Only a tile holding a key this row must not see (the ragged last tile,
             // a causal diagonal) takes the masked path; the others run without any
             // per-element test (a warp-uniform branch, not predication).
@@ -468,6 +501,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                if (direct_store) {
+                    // the rows of this sequence only, 64 bytes per row per step
+                    if (q0 + row < sg.sq) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) +
+                                                               static_cast<size_t>(q_row + row) * p.o_row_stride +
+                                                               static_cast<size_t>(z_q) * D + 32 * cc);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                    continue;
+                }
                 const uint32_t row_addr = s_q + (cc >> 1) * L::Q_BOX_BYTES + row * 128;
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
@@ -476,15 +521,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                                  pk[4 * v + 2], pk[4 * v + 3]);
                 }
             }
-            if (p.lse != nullptr && q0 + row < p.Sq)
-                p.lse[static_cast<size_t>(z_out) * p.Sq + q0 + row] = (m_used + ptx::lg2(l)) * LN2;
+            if (p.lse != nullptr && q0 + row < sg.sq)
+                p.lse[static_cast<size_t>(z_out) * p.Sq + q_row + row] = (m_used + ptx::lg2(l)) * LN2;
             ptx::fence_proxy_async_smem();
         }
         ptx::named_bar_sync(1, 128);
-        if (threadIdx.x == 0 && !*abort_flag) {
+        if (threadIdx.x == 0 && !*abort_flag && !direct_store) {
 #pragma unroll
             for (int c2 = 0; c2 < D / 64; ++c2)
-                ptx::tma_store_3d(&tm_o, s_q + c2 * L::Q_BOX_BYTES, c2 * 64, q0, z_out);
+                ptx::tma_store_3d(&tm_o, s_q + c2 * L::Q_BOX_BYTES, c2 * 64, q_row, z_out);
             ptx::bulk_commit_group();
             ptx::bulk_wait_group_all();
         }
@@ -514,7 +559,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 // with the head-in-group index fastest that holds when G is even.
 inline bool use_pair(const KernelParams &p, int grid)
 {
-    if ((p.debug_flags & DEBUG_SINGLE_CTA) || p.cu_q != nullptr)  // variable-length batches: single-CTA kernel
+    if (p.debug_flags & DEBUG_SINGLE_CTA)
+        return false;
+    // Variable-length batches pair two heads of one group on the same tile (G even), so both CTAs
+    // of a pair always see the same sequence and leave together.
+    if (p.cu_q != nullptr && (p.G % 2) != 0)
         return false;
     if (p.causal && (p.G % 2) != 0)
         return false;

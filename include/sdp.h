@@ -166,8 +166,9 @@ int sdp_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float 
  * down, or give more rows than max_seqlen_q rounded up to a multiple of 128
  * is not computed, and the next sdp_poll_status returns SDP_ERR_BAD_SEQLENS. Inputs must be finite: the key rows after a
  * sequence's last key in its last 128-key tile belong to the next sequence
- * and are read, with weight exactly 0. Every tile runs on the single-CTA
- * kernel; tiles that end past their sequence store O row by row.
+ * and are read, with weight exactly 0. With an even number of query heads per
+ * KV head, tiles run on CTA pairs (two heads of a group on one tile); tiles
+ * that end past their sequence store O row by row.
  */
 int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
                    const int *cu_seqlens_q, const int *cu_seqlens_k, int nseq, int Hq, int Hkv,

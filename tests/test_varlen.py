@@ -89,17 +89,28 @@ def test_small_batches_every_row(w):
     check_every_row(w)
 
 
+@pytest.mark.parametrize("w", [w for w in SMALL if w.Hq // w.Hkv % 2 == 0], ids=lambda w: w.name)
+def test_small_batches_single_cta_kernel(w):
+    """Batches whose groups pair up run on CTA pairs by default; the single-CTA
+    kernel must give the same function."""
+    old = sdp.set_debug_flags(DEBUG_SINGLE_CTA)
+    try:
+        check_every_row(w)
+    finally:
+        sdp.set_debug_flags(old)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_one_sequence_equals_the_dense_call(causal):
-    """A batch of one sequence is sdp_fwd on the transposed layout: the same
-    single-CTA arithmetic per row, so bit for bit."""
+    """A batch of one sequence is sdp_fwd on the transposed layout: with both
+    on the single-CTA kernel the per-row arithmetic is the same, so bit for bit."""
     w = VarlenWorkload("one", (300,), (420,), 8, 2, 128, "fp16", seed=87, causal=causal)
     q, k, v = workloads.make_varlen_inputs(w)
-    o, lse = run(w, q, k, v)
     dev = torch.device("cuda")
     qd, kd, vd = (t.permute(1, 0, 2).unsqueeze(0).contiguous().to(dev) for t in (q, k, v))
     old = sdp.set_debug_flags(DEBUG_SINGLE_CTA)
     try:
+        o, lse = run(w, q, k, v)
         od, ld = sdp.sdp_fwd(qd, kd, vd, scale=w.softmax_scale, causal=causal)
         assert sdp.poll_status() == sdp.SDP_OK
     finally:
