@@ -1,0 +1,52 @@
+"""Failure detection without a GPU fault: every mbarrier wait in the kernels
+is bounded. With the load warp told to issue no copies (debug flag 1),
+nothing ever completes the waits of the MMA issuers and the softmax warps;
+each gives up after the configured limit, records a site code in the status
+word, and the kernel drains, frees tensor memory and returns. The host reads
+SDP_ERR_DEVICE_TIMEOUT from sdp_poll_status, and the context stays usable:
+the next call computes the right result."""
+import pytest
+import torch
+
+import gqa_flash_attention_gb300 as sdp
+import oracle
+from gqa_flash_attention_gb300 import workloads
+from gqa_flash_attention_gb300.workloads import Workload
+from parity import ORACLE_DTYPE, assert_within, compare
+
+pytestmark = pytest.mark.gpu
+
+DEBUG_NO_LOADS = 1
+DEBUG_SINGLE_CTA = 2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gqa_flash_attention_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    sdp.lib()
+
+
+@pytest.mark.parametrize("flags", [DEBUG_NO_LOADS, DEBUG_NO_LOADS | DEBUG_SINGLE_CTA],
+                         ids=["cta_pair", "single_cta"])
+def test_wait_timeout_is_reported_and_the_context_survives(flags):
+    w = Workload("timeout", 1, 4, 2, 256, 384, 128, "fp16", seed=91)  # two heads per group: CTA pairs
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    assert sdp.poll_status() == sdp.SDP_OK
+    old_ms = sdp.set_wait_timeout_ms(50)
+    old_flags = sdp.set_debug_flags(flags)
+    try:
+        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale)
+        assert sdp.poll_status() == sdp.SDP_ERR_DEVICE_TIMEOUT
+        site = sdp.last_status_detail() & 0xFF
+        assert 1 <= site <= 6, hex(sdp.last_status_detail())
+    finally:
+        sdp.set_debug_flags(old_flags)
+        sdp.set_wait_timeout_ms(old_ms)
+    # the status word was cleared and the device still computes correctly
+    assert sdp.poll_status() == sdp.SDP_OK
+    o, lse = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale)
+    assert sdp.poll_status() == sdp.SDP_OK
+    ref_o, ref_l = oracle.sdp_fwd(q.cpu(), k.cpu(), v.cpu(), ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale)
+    assert_within(compare(o, lse, ref_o, ref_l, w.dtype), w.dtype)
