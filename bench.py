@@ -95,10 +95,16 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
-def load_traffic(workload: str):
+def merge_source_hash():
+    import hashlib
+    with open(os.path.join(ROOT, "gqa_flash_attention_gb300", "csrc", "sdp_merge.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic(workload: str, prefix: str = "sdp_fwd_", current_hash=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"sdp_fwd_{workload}_traffic.txt")
+    path = os.path.join(ROOT, "profiles", f"{prefix}{workload}_traffic.txt")
     if not os.path.exists(path):
         return None
     kv = {}
@@ -107,7 +113,7 @@ def load_traffic(workload: str):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-    if kv.get("source_hash") != source_hash():
+    if kv.get("source_hash") != (current_hash or source_hash()):
         return None
     try:
         return int(float(kv["traffic_bytes_per_launch"]))
@@ -547,7 +553,8 @@ def merge_arm(args, w):
         "config": {"workload": f"merge of {P} parts over {w.name} rows", "parts": P, "rows": rows, "D": w.D,
                    "l2": "inputs larger than L2; no flush"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                     "traffic": None, "kernel": "merge_kernel", "bytes_per_launch": nbytes},
+                     "traffic": load_traffic(f"{w.name}_p{P}", "sdp_merge_", merge_source_hash()),
+                     "kernel": "merge_kernel", "bytes_per_launch": nbytes},
         "clocks": clk, "gpu_launches": K}), flush=True)
 
 
