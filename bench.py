@@ -67,6 +67,20 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks (the slowest replica sets the job's time); x itself at N=1."""
+    if dist_env()[0] == 1:
+        return float(x)
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flops_per_replica: float, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every replica does the same work, timed by the slowest."""
+    return world * flops_per_replica / (ms_per_step * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -394,12 +408,8 @@ def ours_arm(args, w):
     if sdp.poll_status() != sdp.SDP_OK:
         raise RuntimeError("kernel reported a timeout in the timed region")
 
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    max_total_ms = float(t.item())
-    ms_per_step = max_total_ms / K
-    value = world * w.flops() / (ms_per_step * 1e-3) / 1e12
+    ms_per_step = max_over_ranks(total_ms, dev) / K
+    value = job_throughput(world, w.flops(), ms_per_step)
 
     # End to end through the public API: every step copies its inputs from pinned host memory and
     # reads O and LSE back to pinned host memory. Steps are pipelined as a serving loop would run
@@ -463,12 +473,10 @@ def ours_arm(args, w):
         torch.cuda.synchronize(dev)
         if sdp.poll_status() != sdp.SDP_OK:
             raise RuntimeError("kernel reported a timeout in the end-to-end leg")
-        te = torch.tensor([e0.elapsed_time(e1) / n_e2e], dtype=torch.float64, device=dev)
-        if world > 1:
-            torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+        te = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
         h2d = sum(t_.numel() * t_.element_size() for t_ in (q_h, k_h, v_h, *cu_h))
         d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
-        e2e = {"value": world * w.flops() / (float(te.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_throughput(world, w.flops(), te), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "pipelined": "copy-in, compute and copy-out streams, two device buffer sets"}
 
