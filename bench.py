@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--op", choices=["attention", "merge"], default="attention",
                     help="merge: time sdp_merge (HBM-bound) on a context-parallel-shaped case instead")
     ap.add_argument("--merge-parts", type=int, default=8)
+    ap.add_argument("--override", nargs="*", default=[], metavar="FIELD=VALUE",
+                    help="change fields of a dense workload (B, Hq, Hkv, Sq, Skv): a smaller case of the same "
+                         "kernel, e.g. for a multi-pass ncu capture; the workload name gets the changes appended")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="replay each step from a CUDA graph (auto: for the split-KV decode workloads, whose "
                          "steps are shorter than the host's per-call work)")
@@ -569,6 +572,16 @@ def merge_arm(args, w):
 def main():
     args = parse()
     w = BENCH_WORKLOADS[args.workload]
+    if args.override:
+        if is_varlen(w):
+            raise SystemExit("--override applies to dense workloads only")
+        kw = {}
+        for item in args.override:
+            key, _, val = item.partition("=")
+            if key not in ("B", "Hq", "Hkv", "Sq", "Skv"):
+                raise SystemExit(f"cannot override {key!r}")
+            kw[key] = int(val)
+        w = w.with_(name=w.name + "_" + "_".join(f"{k}{v}" for k, v in kw.items()), **kw)
     if args.op == "merge":
         merge_arm(args, w)
     elif args.impl == "reference":

@@ -338,3 +338,9 @@ def sdp_fwd_noalloc_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: in
     return int(fn(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.c_void_p(o),
                   ctypes.c_void_p(lse), int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(D), ctypes.c_float(scale),
                   int(dtype), ctypes.c_void_p(stream)))
+
+
+# Short names of the main entry points.
+fwd = sdp_fwd
+fwd_varlen = sdp_fwd_varlen
+merge = sdp_merge

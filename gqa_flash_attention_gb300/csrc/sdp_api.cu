@@ -85,8 +85,8 @@ int device_state(int dev, unsigned int **status)
 
 // 3-D map over a [planes, rows, D] 16-bit tensor; box = 64 columns x box_rows rows
 // x 1 plane with 128-byte swizzle. Rows past `rows` read as zero and are not written.
-int encode_map(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long planes,
-               unsigned box_rows = 128)
+int encode_map_uncached(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long planes,
+                        unsigned box_rows)
 {
     EncodeTiledFn enc = encoder();
     if (enc == nullptr)
@@ -108,8 +108,8 @@ int encode_map(CUtensorMap *map, const void *base, int dtype, int D, long long r
 // 3-D map over a (token, head, dim) 16-bit tensor [rows, heads, D], in the
 // same (column, row, plane) coordinate order as encode_map: plane = head, with
 // a row stride of heads * D elements and a plane stride of D.
-int encode_map_thd(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long heads,
-                   unsigned box_rows = 128)
+int encode_map_thd_uncached(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long heads,
+                            unsigned box_rows)
 {
     EncodeTiledFn enc = encoder();
     if (enc == nullptr)
@@ -126,6 +126,64 @@ int encode_map_thd(CUtensorMap *map, const void *base, int dtype, int D, long lo
     if (r != CUDA_SUCCESS)
         return cuda_fail(cudaErrorInvalidValue);
     return SDP_OK;
+}
+
+// Encoded maps are a pure function of (address, dtype, D, rows, planes, box
+// rows, layout), so repeated calls on the same buffers reuse them instead of
+// re-encoding (a few microseconds of host time per map): a small table,
+// replaced round robin, under its own lock.
+struct MapKey {
+    const void *base;
+    int dtype, D;
+    long long rows, planes;
+    unsigned box_rows;
+    bool thd;
+    bool operator==(const MapKey &o) const
+    {
+        return base == o.base && dtype == o.dtype && D == o.D && rows == o.rows && planes == o.planes &&
+               box_rows == o.box_rows && thd == o.thd;
+    }
+};
+constexpr int kMapCacheSize = 64;
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool valid;
+};
+std::mutex g_map_mu;
+MapEntry g_map_cache[kMapCacheSize] = {};
+int g_map_next = 0;
+
+int encode_cached(CUtensorMap *map, const MapKey &key)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        for (const MapEntry &e : g_map_cache)
+            if (e.valid && e.key == key) {
+                *map = e.map;
+                return SDP_OK;
+            }
+    }
+    const int rc = key.thd ? encode_map_thd_uncached(map, key.base, key.dtype, key.D, key.rows, key.planes, key.box_rows)
+                           : encode_map_uncached(map, key.base, key.dtype, key.D, key.rows, key.planes, key.box_rows);
+    if (rc != SDP_OK)
+        return rc;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    g_map_cache[g_map_next] = MapEntry{key, *map, true};
+    g_map_next = (g_map_next + 1) % kMapCacheSize;
+    return SDP_OK;
+}
+
+int encode_map(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long planes,
+               unsigned box_rows = 128)
+{
+    return encode_cached(map, MapKey{base, dtype, D, rows, planes, box_rows, false});
+}
+
+int encode_map_thd(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long heads,
+                   unsigned box_rows = 128)
+{
+    return encode_cached(map, MapKey{base, dtype, D, rows, heads, box_rows, true});
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -521,6 +579,11 @@ int sdp_version(void) { return 104; }
 
 void sdp_shutdown(void)
 {
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        for (MapEntry &e : g_map_cache)
+            e.valid = false;
+    }
     std::lock_guard<std::mutex> lk(g_mu);
     int cur = 0;
     const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;

@@ -254,7 +254,9 @@ const char *sdp_strerror(int code);
 /* ABI version: 100 * major + minor (101: sdp_fwd_causal; 102: sdp_merge; 103: split-KV; 104: varlen). */
 int sdp_version(void);
 
-/* Free the per-device status words. Call only with no sdp work in flight. */
+/* Free the per-device status words and forget the cached tensor maps (host
+ * copies of TMA descriptors, keyed by buffer address and shape). Call only with
+ * no sdp work in flight. */
 void sdp_shutdown(void);
 
 #ifdef __cplusplus
