@@ -133,9 +133,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     u -= split * units_per_split;
     const int hi = u % p.G;
     u /= p.G;
-    // Causal units do qt + 1 tiles: start the longest ones first.
-    const int qt = p.causal ? p.n_qtiles - 1 - (u % p.n_qtiles) : (u % p.n_qtiles);
-    const int bg = u / p.n_qtiles;
+    int qt, bg;  // query tile; b * Hkv + g
+    if (p.cu_q != nullptr && p.causal) {
+        // Causal variable-length batch: query tile outermost, highest first. A unit of tile qt
+        // reads qt + 1 KV tiles whatever its sequence, so the costliest units start first and the
+        // tiles past shorter sequences (which return at once) come last. (Without the mask a
+        // unit's cost is its sequence's key count, unrelated to qt: the group-major order stays.)
+        const int n_bg = units_per_split / (p.G * p.n_qtiles);
+        qt = p.n_qtiles - 1 - u / n_bg;
+        bg = u % n_bg;
+    } else {
+        // Causal units do qt + 1 tiles: start the longest ones first.
+        qt = p.causal ? p.n_qtiles - 1 - (u % p.n_qtiles) : (u % p.n_qtiles);
+        bg = u / p.n_qtiles;
+    }
     const int b = bg / p.Hkv;
     const int g = bg - b * p.Hkv;
     const bool varlen = p.cu_q != nullptr;
