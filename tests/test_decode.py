@@ -196,3 +196,27 @@ def test_full_size_decode_workloads(name):
     split count), checked on every output row."""
     w = workloads.DECODE_WORKLOADS[name]
     check(w, kv_splits=w.kv_splits)
+
+
+def test_split_kv_replays_from_a_cuda_graph():
+    """Both launches of a split-KV call (attention into the workspace, then the
+    merge) are capturable: a graph replay gives the eager call's result bit for bit."""
+    w = SPLIT[0][0]
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    dt = sdp.SDP_FP16
+    need = sdp.splitkv_workspace_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, dt, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    o_eager, l_eager = sdp.sdp_fwd(q, k, v, kv_splits=0, workspace=ws)
+    o = torch.empty_like(q)
+    lse = torch.empty_like(l_eager)
+    sdp.sdp_fwd(q, k, v, out=o, lse=lse, kv_splits=0, workspace=ws)  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sdp.sdp_fwd(q, k, v, out=o, lse=lse, kv_splits=0, workspace=ws)
+    o.zero_()
+    lse.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert sdp.poll_status() == sdp.SDP_OK
+    assert torch.equal(o, o_eager) and torch.equal(lse, l_eager)

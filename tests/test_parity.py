@@ -173,3 +173,21 @@ def test_causal_single_cta_kernel_every_row(w):
     finally:
         sdp.set_debug_flags(old)
 
+
+
+def test_dense_call_replays_from_a_cuda_graph():
+    w = workloads.WORKLOADS["gqa4_s256_d128_fp16"]
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    o_eager, l_eager = sdp.sdp_fwd(q, k, v)
+    o = torch.empty_like(q)
+    lse = torch.empty_like(l_eager)
+    sdp.sdp_fwd(q, k, v, out=o, lse=lse)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sdp.sdp_fwd(q, k, v, out=o, lse=lse)
+    o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert sdp.poll_status() == sdp.SDP_OK
+    assert torch.equal(o, o_eager) and torch.equal(lse, l_eager)
