@@ -191,3 +191,19 @@ def test_dense_call_replays_from_a_cuda_graph():
     torch.cuda.synchronize()
     assert sdp.poll_status() == sdp.SDP_OK
     assert torch.equal(o, o_eager) and torch.equal(lse, l_eager)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_large_scores_saturate_cleanly(dtype):
+    """Inputs scaled by 24 so the scaled scores reach the thousands: almost every weight
+    underflows to exactly 0 and each row copies (nearly) one V row; nothing
+    overflows in the fp32 scaling, exponentials or sums."""
+    w = Workload(f"large_{dtype}", 1, 4, 2, 200, 700, 128, dtype, seed=97)
+    q, k, v = workloads.make_inputs(w)
+    q, k = (q.float() * 24).to(q.dtype), (k.float() * 24).to(k.dtype)
+    o, lse = gpu_run(q, k, v, w.softmax_scale)
+    ref_o, ref_l = oracle.sdp_fwd(q, k, v, ORACLE_DTYPE[dtype], w.shape, w.softmax_scale)
+    st = compare(o, lse, ref_o, ref_l, dtype)
+    assert st["nan_o"] == 0 and st["nan_lse"] == 0
+    assert st["max_abs"] <= (2e-2 if dtype == "fp16" else 4e-2), st
+    assert st["lse_max_abs"] <= 1e-6 * max(1.0, float(np.abs(ref_l).max())) * 8, st
