@@ -295,7 +295,11 @@ def kernel_name(w):
     """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
     the units of each (batch, KV head) pair up (and, causal, share the query
     tile), else the single-CTA kernel; split-KV adds the merge kernel;
-    variable-length batches pair up when the group size is even."""
+    variable-length batches pair up when the group size is even; head dim 128
+    always runs on single CTAs."""
+    if w.D == 128:
+        name = "sdp_fwd_kernel"  # the single-CTA kernel is as fast or faster at D=128
+        return name + " + merge_kernel" if getattr(w, "kv_splits", 1) != 1 else name
     if is_varlen(w):
         return "sdp_fwd_pair_kernel" if (w.Hq // w.Hkv) % 2 == 0 else "sdp_fwd_kernel"
     sq, G = launch_shape(w)

@@ -6,7 +6,7 @@ namespace sdp {
 
 cudaError_t launch_d256_bf16(const LaunchMaps &m, const KernelParams &p, int grid, cudaStream_t stream)
 {
-    if (use_pair(p, grid))
+    if (use_pair(p, grid, 256))
         return launch_sdp_fwd_pair<256, true>(m.q, m.k_half, m.v, m.o, p, grid, stream);
     return launch_sdp_fwd<256, true>(m.q, m.k, m.v, m.o, p, grid, stream);
 }

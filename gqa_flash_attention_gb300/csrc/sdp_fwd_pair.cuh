@@ -568,9 +568,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 // (batch, KV head), query tiles x heads per group, are even in number.
 // Causal units of one pair must also share the query tile (same tile count):
 // with the head-in-group index fastest that holds when G is even.
-inline bool use_pair(const KernelParams &p, int grid)
+inline bool use_pair(const KernelParams &p, int grid, int D)
 {
     if (p.debug_flags & DEBUG_SINGLE_CTA)
+        return false;
+    // At D=128 the single-CTA kernel measured as fast or faster (GQA with 4 heads per group: +5 %;
+    // MHA: within 2 %): a 128-key tile there is half the tensor work of D=256, the softmax takes
+    // the larger share, and the pair's halved K/V traffic per SM buys little.
+    if (D == 128 && !(p.debug_flags & DEBUG_PAIR_D128))
         return false;
     // Variable-length batches pair two heads of one group on the same tile (G even), so both CTAs
     // of a pair always see the same sequence and leave together.

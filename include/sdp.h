@@ -241,7 +241,9 @@ unsigned int sdp_set_wait_timeout_ms(unsigned int ms);
  * through its timeout path (used to test that path without a fault). Bit 1:
  * always run the single-CTA kernel, never the CTA-pair kernel (both compute
  * the same result; tests compare them). Bit 2: never pack the query heads of
- * a group into one head (same result; tests compare). Returns the previous flags.
+ * a group into one head (same result; tests compare). Bit 3: at head dim 128,
+ * use the CTA-pair kernel where it qualifies (by default head dim 128 runs on
+ * single CTAs, which measured as fast or faster there). Returns the previous flags.
  */
 int sdp_set_debug_flags(int flags);
 

@@ -87,6 +87,30 @@ def test_single_cta_kernel_every_row(w):
         sdp.set_debug_flags(old)
 
 
+DEBUG_PAIR_D128 = 8
+
+
+@pytest.mark.parametrize("w", [w for w in SMALL if w.D == 128 and not w.name.startswith("one_")],
+                         ids=lambda w: w.name)
+def test_pair_kernel_at_d128_every_row(w):
+    """Head dim 128 runs on single CTAs by default; the CTA-pair kernel, kept
+    for it behind a flag, must give the same function."""
+    old = sdp.set_debug_flags(DEBUG_PAIR_D128)
+    try:
+        check_full(w)
+    finally:
+        sdp.set_debug_flags(old)
+
+
+@pytest.mark.parametrize("name", ["gqa4_b2_s8k_d128_bf16_peaky", "mha_b4_s16k_d128_fp16"])
+def test_pair_kernel_at_d128_full_size_sampled(name):
+    old = sdp.set_debug_flags(DEBUG_PAIR_D128)
+    try:
+        test_full_size_workload_sampled_rows(name)
+    finally:
+        sdp.set_debug_flags(old)
+
+
 def test_smallest_workload_every_row():
     check_full(workloads.WORKLOADS["gqa4_s256_d128_fp16"])
 

@@ -21,6 +21,7 @@ from parity import ORACLE_DTYPE, assert_within, compare
 pytestmark = pytest.mark.gpu
 
 DEBUG_SINGLE_CTA = 2
+DEBUG_PAIR_D128 = 8
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -89,11 +90,12 @@ def test_small_batches_every_row(w):
     check_every_row(w)
 
 
+@pytest.mark.parametrize("flags", [DEBUG_SINGLE_CTA, DEBUG_PAIR_D128], ids=["single_cta", "pair_at_d128"])
 @pytest.mark.parametrize("w", [w for w in SMALL if w.Hq // w.Hkv % 2 == 0], ids=lambda w: w.name)
-def test_small_batches_single_cta_kernel(w):
-    """Batches whose groups pair up run on CTA pairs by default; the single-CTA
-    kernel must give the same function."""
-    old = sdp.set_debug_flags(DEBUG_SINGLE_CTA)
+def test_small_batches_other_kernel(w, flags):
+    """Batches whose groups pair up run on CTA pairs by default at D=256 and on
+    single CTAs at D=128; the other kernel must give the same function."""
+    old = sdp.set_debug_flags(flags)
     try:
         check_every_row(w)
     finally:
