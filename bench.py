@@ -275,7 +275,8 @@ def reference_arm(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.median(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_of(w, args.gpus),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
+                         "extrapolated_full_workload_s": w.flops() / (value * 1e12)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -516,6 +517,7 @@ def ours_arm(args, w):
         rows = args.cpu_rows or cpu_rows_auto(w)
         tf, sec, desc, threads = run_cpu_oracle(w, rows, q_h, k_h, v_h)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "extrapolated_full_workload_s": w.flops() / (tf * 1e12),
                "sample": f"{desc} ({sec:.1f} s)"}
 
     cfg = config_of(w, world)
