@@ -101,21 +101,30 @@ def load_hbm_peak():
     return 6800.0, "fallback"
 
 
+def code_tokens(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed: what the compiler sees, so a
+    comment edit does not count as a kernel change."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash():
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gqa_flash_attention_gb300", "csrc")
     # the kernel's own sources only (the host-side entry points do not change its traffic)
     for name in sorted(n for n in os.listdir(csrc) if n.startswith(("sdp_fwd", "ptx", "sdp_launch"))):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name)) as f:
+            h.update(name.encode() + code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 
 def merge_source_hash():
     import hashlib
-    with open(os.path.join(ROOT, "gqa_flash_attention_gb300", "csrc", "sdp_merge.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(os.path.join(ROOT, "gqa_flash_attention_gb300", "csrc", "sdp_merge.cu")) as f:
+        return hashlib.sha256(code_tokens(f.read()).encode()).hexdigest()[:16]
 
 
 def load_traffic(workload: str, prefix: str = "sdp_fwd_", current_hash=None):

@@ -4,7 +4,7 @@
 // CTAs on two SMs form a cluster and share every K/V tile: each CTA keeps its
 // own unit (128 query rows, its S/P buffers and its O accumulator in its own
 // tensor memory) while the tensor cores of both SMs run one M=256 MMA per
-// k-step, issued by a single thread of the leader CTA (rank 0).
+// k-step, issued by the leader CTA's (rank 0) two issuer warps.
 //
 //   S = Q K^T  : M=256 (128 rows per CTA), N=128 keys; CTA r holds keys
 //                [64r, 64r+64) of the tile (half of B, K-major).
@@ -12,9 +12,10 @@
 //                value columns [rD/2, rD/2 + D/2) of the tile (half of B,
 //                N-major).
 //
-// Each SM therefore receives half of every K and V tile from L2: the single
-// CTA kernel is bound by that stream (about 43 B/clk per SM), which this
-// halves; the leader also issues half as many MMA instructions per FLOP.
+// Each SM therefore receives half of every K and V tile from L2: at D=256 the
+// single-CTA kernel is bound by that stream (about 43 B/clk per SM), which this
+// halves; the leader also issues half as many MMA instructions per FLOP. (At
+// D=128 the single-CTA kernel measured as fast or faster and is the default.)
 //
 // Cross-CTA protocol (barriers live in each CTA at the same offsets):
 //   q_full, slot_full : armed by the leader's producer for both halves; both
@@ -23,9 +24,11 @@
 //                       multicast to both CTAs.
 //   p_full            : in the leader; one arrival per softmax warp of both
 //                       CTAs (the peer's arrive remotely).
-// Both CTAs must belong to the same (batch, KV head): the launcher only pairs
-// units when each (batch, KV head) has an even number of units (query tiles x
-// query heads per group); otherwise it runs the single-CTA kernel.
+// Both CTAs must belong to the same (batch, KV head) and, in a variable-length
+// batch, the same sequence and query tile: the launcher only pairs units when
+// each (batch, KV head) has an even number of units (query tiles x query heads
+// per group; an even group size for causal and variable-length launches);
+// otherwise it runs the single-CTA kernel.
 #pragma once
 
 #include "sdp_fwd_kernel.cuh"
