@@ -120,6 +120,14 @@ def test_scale_sign_and_zero(scale):
     check_full(Workload("scale", 1, 4, 2, 150, 260, 128, "fp16", seed=41, scale=scale))
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.0625])
+@pytest.mark.parametrize("causal", [False, True])
+def test_scale_sign_and_zero_on_cta_pairs(scale, causal):
+    """256 query rows of two heads per group at D=256 (no head packing): CTA
+    pairs, whose row extreme is a minimum when the scale is negative."""
+    check_full(Workload("scale_pair", 1, 4, 2, 256, 260, 256, "bf16", seed=46, scale=scale, causal=causal))
+
+
 def test_peaky_keys_small():
     check_full(Workload("peaky", 1, 8, 2, 256, 1024, 128, "bf16", seed=42, peaky_k=True))
 
