@@ -84,12 +84,14 @@ struct Layout {
     static_assert(O_DONE_RING >= NSBUF + 1, "PV completion ring must outrun the S buffers");
     // An issuer waiting on the chunk at load position P reads slot P % NSLOTS by
     // parity, which is only sound if the chunk at P - NSLOTS has landed. The
-    // S issuer at K_t has seen PV_{t-NSBUF} complete and every earlier K, so the
-    // only chunks before K_t that may still be in flight belong to V_{t-2}
-    // (NSBUF = 3); the PV issuer at V_j has seen S_j, so only K_{j+1} may be in
-    // flight. Neither sits exactly NSLOTS before the waited chunk when
-    // NSLOTS >= 2 * CHUNKS_PER_TILE and NSBUF <= 3.
-    static_assert(NSLOTS >= 2 * CHUNKS_PER_TILE && NSBUF <= 3, "ring parity soundness");
+    // S issuer waits for K_t before PV_{t-NSBUF}, having seen PV_{t-NSBUF-1}
+    // complete and every earlier K land, so only V_{t-NSBUF} .. V_{t-2} may be
+    // in flight. The PV issuer waits for V_j having seen S_{j-1} complete (one
+    // chunk per tile: before P_j is ready) or S_j (two: after), and every
+    // earlier V, so only K_j and K_{j+1} (resp. K_{j+1}) may be in flight. With
+    // one chunk per tile and NSBUF <= 3, or two chunks and NSBUF = 2, each of
+    // those sits 1 to 3 positions before the waited chunk, never NSLOTS >= 4.
+    static_assert(NSLOTS >= 4 && (CHUNKS_PER_TILE == 1 ? NSBUF <= 3 : NSBUF == 2), "ring parity soundness");
 };
 
 // Lazy rescale threshold in base-2 units: the running maximum is only moved
@@ -388,6 +390,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool issued = false;
             bool ok = __all_sync(0xffffffffu, wait_bounded(q_full, 0, cx, SITE_Q_FULL));
             for (int t = 0; ok && t < n; ++t) {
+                const int p0 = pos_k<CPT>(t);
+                // K_t has usually landed long before PV_{t-NB} completes, so its
+                // slots are waited for first, off the PV_{t-NB} -> S_t path.
+#pragma unroll
+                for (int ch = 0; ch < CPT; ++ch) {
+                    const int pos = p0 + ch;
+                    if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * (pos % NS), (pos / NS) & 1, cx, SITE_SLOT_FULL))))
+                        break;
+                }
+                if (!ok)
+                    break;
                 if (t >= NB) {  // buffer t % NB held P_{t-NB}: PV_{t-NB} must have read it
                     const int pv = t - NB;
                     ok = __all_sync(0xffffffffu, wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx,
@@ -395,15 +408,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!ok)
                         break;
                 }
+                ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + L::TM_S + (t % NB) * L::BN;
-                const int p0 = pos_k<CPT>(t);
 #pragma unroll
                 for (int ch = 0; ch < CPT; ++ch) {
                     const int pos = p0 + ch;
                     const int slot = pos % NS;
-                    if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
-                        break;
-                    ptx::tc_fence_after();
                     const uint64_t kslot = dk + static_cast<uint64_t>((slot * L::CHUNK_BYTES) >> 4);
                     const uint64_t qch = dq + static_cast<uint64_t>((2 * ch * L::BOX_BYTES) >> 4);
 #pragma unroll
@@ -414,8 +424,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     issued = true;
                     ptx::mma_commit_w(slot_empty0 + 8u * slot);
                 }
-                if (!ok)
-                    break;
                 ptx::mma_commit_w(s_full0 + 8u * (t % NB));
             }
             if (issued) {  // all of this thread's MMAs complete before TMEM is freed
@@ -431,18 +439,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int j = 0; ok && j < n; ++j) {
                 const int buf = j % NB;
+                const int p0 = pos_v<CPT>(j, n);
+                // With one ring chunk per tile, V_j has usually landed before P_j is
+                // ready, so its slot is waited for first, off the P_j -> PV_j path.
+                // (With two, the chunk NSLOTS before V_j's first can belong to K_j,
+                // which only P_j being ready shows to have landed: that order stays.)
+                if constexpr (CPT == 1) {
+                    if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * (p0 % NS), (p0 / NS) & 1, cx, SITE_SLOT_FULL))))
+                        break;
+                }
                 if (!(ok = __all_sync(0xffffffffu, wait_bounded(p_full0 + 8u * buf, (j / NB) & 1, cx, SITE_P_FULL))))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t a_tmem = tmem + L::TM_S + buf * L::BN;
-                const int p0 = pos_v<CPT>(j, n);
 #pragma unroll
                 for (int ch = 0; ch < CPT; ++ch) {
                     const int pos = p0 + ch;
                     const int slot = pos % NS;
-                    if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
-                        break;
-                    ptx::tc_fence_after();
+                    if constexpr (CPT != 1) {
+                        if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
+                            break;
+                        ptx::tc_fence_after();
+                    }
                     const uint64_t vslot = dv + static_cast<uint64_t>((slot * L::CHUNK_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)

@@ -62,7 +62,7 @@ struct PairLayout {
     static_assert(O_DONE_RING >= NSBUF + 1, "PV completion ring must outrun the S buffers");
     // Same parity-soundness argument as the single-CTA ring, with one slot per
     // half tile (so CHUNKS_PER_TILE = 1).
-    static_assert(NSLOTS >= 2 && NSBUF <= 3, "ring parity soundness");
+    static_assert(NSLOTS >= 4 && NSBUF <= 3, "ring parity soundness");
 };
 
 // Slow path for a wait whose phase is completed by arrivals from the peer CTA.
@@ -288,6 +288,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             bool issued = false;
             bool ok = __all_sync(0xffffffffu, wait_bounded(q_full, 0, cx, SITE_Q_FULL));
             for (int t = 0; ok && t < n; ++t) {
+                // K_t first (it has usually landed), then PV_{t-NB}: the slot wait
+                // stays off the PV_{t-NB} -> S_t path.
+                const int pos = pos_k<1>(t);
+                const int slot = pos % NS;
+                if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
+                    break;
                 if (t >= NB) {
                     const int pv = t - NB;
                     ok = __all_sync(0xffffffffu, wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx,
@@ -295,10 +301,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     if (!ok)
                         break;
                 }
-                const int pos = pos_k<1>(t);
-                const int slot = pos % NS;
-                if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
-                    break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + L::TM_S + (t % NB) * L::BN;
                 const uint64_t kslot = dk + static_cast<uint64_t>((slot * L::HALF_BYTES) >> 4);
@@ -325,12 +327,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int j = 0; ok && j < n; ++j) {
                 const int buf = j % NB;
-                if (!(ok = __all_sync(0xffffffffu, wait_bounded(p_full0 + 8u * buf, (j / NB) & 1, cx, SITE_P_FULL))))
-                    break;
-                ptx::tc_fence_after();
+                // V_j first (it has usually landed), then P_j: the slot wait stays
+                // off the P_j -> PV_j path.
                 const int pos = pos_v<1>(j, n);
                 const int slot = pos % NS;
                 if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
+                    break;
+                if (!(ok = __all_sync(0xffffffffu, wait_bounded(p_full0 + 8u * buf, (j / NB) & 1, cx, SITE_P_FULL))))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t a_tmem = tmem + L::TM_S + buf * L::BN;
