@@ -487,13 +487,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float c = p.c;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
+        bool s_seen = false;  // S_j's barrier was seen complete while tile j-1 ended
 
         for (int j = 0; j < n; ++j) {
             const int buf = j % NB;
-            ok = wait_bounded(s_full0 + 8u * buf, (j / NB) & 1, cx, SITE_S_FULL);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok)
-                break;
+            if (!__all_sync(0xffffffffu, s_seen)) {
+                ok = wait_bounded(s_full0 + 8u * buf, (j / NB) & 1, cx, SITE_S_FULL);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok)
+                    break;
+            }
             ptx::tc_fence_after();
             const uint32_t ts = t_s + buf * L::BN;
             uint32_t sr[128];
@@ -580,6 +583,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 exp_tile(std::true_type{});
             else
                 exp_tile(std::false_type{});
+            // Poll S_{j+1}'s barrier now, so the answer returns while P_j is stored
+            // and handed off (no parity aliasing: S_j complete implies
+            // S_{j+1-NSBUF} complete, and S_{j+1+NSBUF} waits for P_{j+1}).
+            s_seen = j + 1 < n && ptx::mbar_test_wait(s_full0 + 8u * ((j + 1) % NB), ((j + 1) / NB) & 1);
             float sum0, sum1, sum2, sum3;
             ptx::f2_unpack(sum01, sum0, sum1);
             ptx::f2_unpack(sum23, sum2, sum3);
