@@ -48,7 +48,7 @@ struct PairLayout {
     static constexpr int BAR_AREA = 512;
     static constexpr int NSLOTS = (SMEM_LIMIT - BAR_AREA - 1024 - Q_BYTES) / HALF_BYTES;
     static constexpr int NSBUF = (D == 128) ? 3 : 2;
-    static constexpr int NBARS = 1 + 2 * NSLOTS + 2 * NSBUF + O_DONE_RING + 2;
+    static constexpr int NBARS = 1 + 2 * NSLOTS + 3 * NSBUF + O_DONE_RING + 2;
     static constexpr int BAR_OFF = Q_BYTES + NSLOTS * HALF_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFF + BAR_AREA + 1024;
     static constexpr int TM_O = 0;
@@ -121,6 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t p_full0 = bar0 + 8u * (1 + 2 * NS + NB);
     const uint32_t o_done0 = bar0 + 8u * (1 + 2 * NS + 2 * NB);
     const uint32_t final0 = bar0 + 8u * (1 + 2 * NS + 2 * NB + O_DONE_RING);
+    const uint32_t p_half0 = final0 + 16u;  // the first 64 keys of P_j are in tensor memory
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
@@ -201,6 +202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < NB; ++i) {
             ptx::mbar_init(s_full0 + 8u * i, 1);
             ptx::mbar_init(p_full0 + 8u * i, L::P_ARRIVALS);
+            ptx::mbar_init(p_half0 + 8u * i, L::P_ARRIVALS);
         }
         for (int i = 0; i < O_DONE_RING; ++i)
             ptx::mbar_init(o_done0 + 8u * i, 1);
@@ -333,16 +335,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 const int slot = pos % NS;
                 if (!(ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL))))
                     break;
-                if (!(ok = __all_sync(0xffffffffu, wait_bounded(p_full0 + 8u * buf, (j / NB) & 1, cx, SITE_P_FULL))))
-                    break;
-                ptx::tc_fence_after();
                 const uint32_t a_tmem = tmem + L::TM_S + buf * L::BN;
                 const uint64_t vslot = dv + static_cast<uint64_t>((slot * L::HALF_BYTES) >> 4);
+                // keys 0-63 of P_j (K steps 0-3) as soon as that half is in tensor memory,
+                // then keys 64-127
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    ptx::mma_ts_pair_w(tmem + L::TM_O, a_tmem + kk * 8, vslot + ((kk * 2048) >> 4), IDESC_PV,
-                                     (j > 0) || (kk > 0));
-                issued = true;
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t bar = (h == 0 ? p_half0 : p_full0) + 8u * buf;
+                    if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar, (j / NB) & 1, cx, SITE_P_FULL))))
+                        break;
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                        ptx::mma_ts_pair_w(tmem + L::TM_O, a_tmem + kk * 8, vslot + ((kk * 2048) >> 4), IDESC_PV,
+                                         (j > 0) || (kk > 0));
+                    issued = true;
+                }
+                if (!ok)
+                    break;
                 ptx::mma_commit_pair_w(slot_empty0 + 8u * slot);
                 ptx::mma_commit_pair_w(o_done0 + 8u * (j % O_DONE_RING));
             }
@@ -357,7 +367,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
         const uint32_t t_s = tmem + lane_off + L::TM_S;
         const uint32_t t_o = tmem + lane_off + L::TM_O;
-        const uint32_t p_full_leader = ptx::map_to_rank(p_full0, 0);
         const float c = p.c;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
@@ -425,12 +434,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
             // p = 2^(s * c - m), two elements per f32x2 instruction for the scaling
             // and the running sums (each lane rounds exactly as fmaf / + would).
+            // P_j is handed over in two 64-key halves, so PV_j's first four MMAs can
+            // start while the second half is computed.
             uint32_t pk[64];
             const uint64_t c2 = ptx::f2_pack(c, c), negm2 = ptx::f2_pack(neg_m, neg_m);
             uint64_t sum01 = ptx::f2_pack(0.f, 0.f), sum23 = sum01;
-            auto exp_tile = [&](auto masked) {
+            auto exp_half = [&](auto masked, auto half) {
+                constexpr int H = decltype(half)::value;
 #pragma unroll
-                for (int i = 0; i < 64; i += 2) {
+                for (int i = 32 * H; i < 32 * H + 32; i += 2) {
                     float x0, x1, x2, x3;
                     ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i], s[2 * i + 1]), c2, negm2), x0, x1);
                     ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i + 2], s[2 * i + 3]), c2, negm2), x2, x3);
@@ -450,21 +462,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     pk[i + 1] = pack2<BF16>(p2, p3);
                 }
             };
+            // One arrival per warp on the leader's barrier, after every lane's TMEM writes.
+            auto hand_over = [&](uint32_t bar) {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader)
+                        ptx::mbar_arrive(bar);
+                    else
+                        ptx::mbar_arrive_cluster(ptx::map_to_rank(bar, 0));
+                }
+            };
             if (tail)
-                exp_tile(std::true_type{});
+                exp_half(std::true_type{}, std::integral_constant<int, 0>{});
             else
-                exp_tile(std::false_type{});
-            float sum0, sum1, sum2, sum3;
-            ptx::f2_unpack(sum01, sum0, sum1);
-            ptx::f2_unpack(sum23, sum2, sum3);
+                exp_half(std::false_type{}, std::integral_constant<int, 0>{});
             ptx::tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            ptx::tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
             ptx::tmem_wait_st();
-            const float tile_sum = (sum0 + sum1) + (sum2 + sum3);
-            l = (j == 0) ? tile_sum : fmaf(l, alpha, tile_sum);
 
             // Same lazy-rescale rule and aliasing argument as the single-CTA kernel:
-            // S_j completing implies PV_{j-NSBUF} completed.
+            // S_j completing implies PV_{j-NSBUF} completed. O is rescaled before the
+            // first half of P_j is handed over (PV_j starts accumulating then).
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 const int pv = j - 1;
                 ok = wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx, SITE_O_DONE);
@@ -484,15 +502,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 }
                 ptx::tmem_wait_st();
             }
-            // One arrival per warp on the leader's p_full, after every lane's TMEM writes.
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (leader)
-                    ptx::mbar_arrive(p_full0 + 8u * buf);
-                else
-                    ptx::mbar_arrive_cluster(p_full_leader + 8u * buf);
-            }
+            hand_over(p_half0 + 8u * buf);
+
+            if (tail)
+                exp_half(std::true_type{}, std::integral_constant<int, 1>{});
+            else
+                exp_half(std::false_type{}, std::integral_constant<int, 1>{});
+            ptx::tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            ptx::tmem_wait_st();
+            hand_over(p_full0 + 8u * buf);
+            float sum0, sum1, sum2, sum3;
+            ptx::f2_unpack(sum01, sum0, sum1);
+            ptx::f2_unpack(sum23, sum2, sum3);
+            const float tile_sum = (sum0 + sum1) + (sum2 + sum3);
+            l = (j == 0) ? tile_sum : fmaf(l, alpha, tile_sum);
             m_used = m_new;
         }
 
