@@ -48,13 +48,15 @@ struct PairLayout {
     static constexpr int BAR_AREA = 512;
     static constexpr int NSLOTS = (SMEM_LIMIT - BAR_AREA - 1024 - Q_BYTES) / HALF_BYTES;
     static constexpr int NSBUF = (D == 128) ? 3 : 2;
-    static constexpr int NBARS = 1 + 2 * NSLOTS + 3 * NSBUF + O_DONE_RING + 2;
+    static constexpr int P_ARRIVALS = 8;                 // 4 softmax warps in each CTA
+    static constexpr int P_PARTS = 4;                    // P_j handed over in parts of 128 / P_PARTS keys
+    static_assert(P_PARTS == 2 || P_PARTS == 4, "P hand-off parts");
+    static constexpr int NBARS = 1 + 2 * NSLOTS + (1 + P_PARTS) * NSBUF + O_DONE_RING + 2;
     static constexpr int BAR_OFF = Q_BYTES + NSLOTS * HALF_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFF + BAR_AREA + 1024;
     static constexpr int TM_O = 0;
     static constexpr int TM_S = D;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int P_ARRIVALS = 8;                 // 4 softmax warps in each CTA
     static_assert(D == 128 || D == 256, "head dim");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
     static_assert(D + NSBUF * BN <= TMEM_COLS, "tensor memory");
@@ -121,7 +123,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t p_full0 = bar0 + 8u * (1 + 2 * NS + NB);
     const uint32_t o_done0 = bar0 + 8u * (1 + 2 * NS + 2 * NB);
     const uint32_t final0 = bar0 + 8u * (1 + 2 * NS + 2 * NB + O_DONE_RING);
-    const uint32_t p_half0 = final0 + 16u;  // the first 64 keys of P_j are in tensor memory
+    // part q < P_PARTS - 1 of P_j is in tensor memory: p_part0 + 8 * (NB * q + buf); the last part is p_full
+    const uint32_t p_part0 = final0 + 16u;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
@@ -202,7 +205,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < NB; ++i) {
             ptx::mbar_init(s_full0 + 8u * i, 1);
             ptx::mbar_init(p_full0 + 8u * i, L::P_ARRIVALS);
-            ptx::mbar_init(p_half0 + 8u * i, L::P_ARRIVALS);
+            for (int q = 0; q + 1 < L::P_PARTS; ++q)
+                ptx::mbar_init(p_part0 + 8u * (NB * q + i), L::P_ARRIVALS);
         }
         for (int i = 0; i < O_DONE_RING; ++i)
             ptx::mbar_init(o_done0 + 8u * i, 1);
@@ -337,16 +341,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     break;
                 const uint32_t a_tmem = tmem + L::TM_S + buf * L::BN;
                 const uint64_t vslot = dv + static_cast<uint64_t>((slot * L::HALF_BYTES) >> 4);
-                // keys 0-63 of P_j (K steps 0-3) as soon as that half is in tensor memory,
-                // then keys 64-127
+                // each part of P_j's keys (8 / P_PARTS K steps) as soon as it is in tensor memory
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t bar = (h == 0 ? p_half0 : p_full0) + 8u * buf;
+                for (int h = 0; h < L::P_PARTS; ++h) {
+                    const uint32_t bar = h + 1 < L::P_PARTS ? p_part0 + 8u * (NB * h + buf) : p_full0 + 8u * buf;
                     if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar, (j / NB) & 1, cx, SITE_P_FULL))))
                         break;
                     ptx::tc_fence_after();
+                    constexpr int KS = 8 / L::P_PARTS;
 #pragma unroll
-                    for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                    for (int kk = KS * h; kk < KS * h + KS; ++kk)
                         ptx::mma_ts_pair_w(tmem + L::TM_O, a_tmem + kk * 8, vslot + ((kk * 2048) >> 4), IDESC_PV,
                                          (j > 0) || (kk > 0));
                     issued = true;
@@ -434,15 +438,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
             // p = 2^(s * c - m), two elements per f32x2 instruction for the scaling
             // and the running sums (each lane rounds exactly as fmaf / + would).
-            // P_j is handed over in two 64-key halves, so PV_j's first four MMAs can
-            // start while the second half is computed.
+            // P_j is handed over in P_PARTS parts of consecutive keys, so PV_j's first
+            // MMAs start while the softmax computes the later parts.
+            constexpr int PW = 64 / L::P_PARTS;  // packed 16-bit pairs (32-bit words) per part
             uint32_t pk[64];
             const uint64_t c2 = ptx::f2_pack(c, c), negm2 = ptx::f2_pack(neg_m, neg_m);
             uint64_t sum01 = ptx::f2_pack(0.f, 0.f), sum23 = sum01;
-            auto exp_half = [&](auto masked, auto half) {
-                constexpr int H = decltype(half)::value;
+            auto exp_part = [&](auto masked, auto part) {
+                constexpr int Q = decltype(part)::value;
 #pragma unroll
-                for (int i = 32 * H; i < 32 * H + 32; i += 2) {
+                for (int i = PW * Q; i < PW * Q + PW; i += 2) {
                     float x0, x1, x2, x3;
                     ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i], s[2 * i + 1]), c2, negm2), x0, x1);
                     ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i + 2], s[2 * i + 3]), c2, negm2), x2, x3);
@@ -462,6 +467,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     pk[i + 1] = pack2<BF16>(p2, p3);
                 }
             };
+            // exponentials of one part, stored to its columns of S_j's buffer
+            auto compute_part = [&](auto part) {
+                constexpr int Q = decltype(part)::value;
+                if (tail)
+                    exp_part(std::true_type{}, part);
+                else
+                    exp_part(std::false_type{}, part);
+                if constexpr (PW == 16)
+                    ptx::tmem_st16(ts + 16 * Q, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * Q]));
+                else
+                    ptx::tmem_st32(ts + 32 * Q, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * Q]));
+                ptx::tmem_wait_st();
+            };
             // One arrival per warp on the leader's barrier, after every lane's TMEM writes.
             auto hand_over = [&](uint32_t bar) {
                 ptx::tc_fence_before();
@@ -473,16 +491,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                         ptx::mbar_arrive_cluster(ptx::map_to_rank(bar, 0));
                 }
             };
-            if (tail)
-                exp_half(std::true_type{}, std::integral_constant<int, 0>{});
-            else
-                exp_half(std::false_type{}, std::integral_constant<int, 0>{});
-            ptx::tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            ptx::tmem_wait_st();
+            auto part_bar = [&](int q) { return q + 1 < L::P_PARTS ? p_part0 + 8u * (NB * q + buf) : p_full0 + 8u * buf; };
+            compute_part(std::integral_constant<int, 0>{});
 
             // Same lazy-rescale rule and aliasing argument as the single-CTA kernel:
             // S_j completing implies PV_{j-NSBUF} completed. O is rescaled before the
-            // first half of P_j is handed over (PV_j starts accumulating then).
+            // first part of P_j is handed over (PV_j starts accumulating then).
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 const int pv = j - 1;
                 ok = wait_bounded(o_done0 + 8u * (pv % O_DONE_RING), (pv / O_DONE_RING) & 1, cx, SITE_O_DONE);
@@ -502,15 +516,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 }
                 ptx::tmem_wait_st();
             }
-            hand_over(p_half0 + 8u * buf);
-
-            if (tail)
-                exp_half(std::true_type{}, std::integral_constant<int, 1>{});
-            else
-                exp_half(std::false_type{}, std::integral_constant<int, 1>{});
-            ptx::tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-            ptx::tmem_wait_st();
-            hand_over(p_full0 + 8u * buf);
+            hand_over(part_bar(0));
+            compute_part(std::integral_constant<int, 1>{});
+            hand_over(part_bar(1));
+            if constexpr (L::P_PARTS == 4) {
+                compute_part(std::integral_constant<int, 2>{});
+                hand_over(part_bar(2));
+                compute_part(std::integral_constant<int, 3>{});
+                hand_over(part_bar(3));
+            }
             float sum0, sum1, sum2, sum3;
             ptx::f2_unpack(sum01, sum0, sum1);
             ptx::f2_unpack(sum23, sum2, sum3);
