@@ -22,8 +22,14 @@
 //                       CTAs' TMA loads complete on the leader's barrier.
 //   slot_empty, s_full, o_done : arrived by the leader's MMA commits,
 //                       multicast to both CTAs.
-//   p_full            : in the leader; one arrival per softmax warp of both
-//                       CTAs (the peer's arrive remotely).
+//   p_part, p_full    : in the leader; one arrival per softmax warp of both
+//                       CTAs (the peer's arrive remotely) per part of P_j.
+//                       P_j is handed over in P_PARTS parts of consecutive
+//                       keys (p_part for all but the last, p_full for the
+//                       last), and the PV issuer runs each part's K steps as
+//                       soon as it arrives: the S_j -> softmax_j -> PV_j ->
+//                       S_{j+NSBUF} chain that bounds this kernel then keeps
+//                       only the last part's MMAs after the softmax ends.
 // Both CTAs must belong to the same (batch, KV head) and, in a variable-length
 // batch, the same sequence and query tile: the launcher only pairs units when
 // each (batch, KV head) has an even number of units (query tiles x query heads
