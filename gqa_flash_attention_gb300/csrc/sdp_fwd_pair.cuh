@@ -55,8 +55,12 @@ struct PairLayout {
     static constexpr int NSLOTS = (SMEM_LIMIT - BAR_AREA - 1024 - Q_BYTES) / HALF_BYTES;
     static constexpr int NSBUF = (D == 128) ? 3 : 2;
     static constexpr int P_ARRIVALS = 8;                 // 4 softmax warps in each CTA
-    static constexpr int P_PARTS = 4;                    // P_j handed over in parts of 128 / P_PARTS keys
-    static_assert(P_PARTS == 2 || P_PARTS == 4, "P hand-off parts");
+    // P_j is handed over in parts of 128 / P_PARTS keys. Each part costs a hand-off
+    // (fence, warp sync, one arrival per warp, remote from the peer): at D=256 the
+    // S -> softmax -> PV chain bounds the kernel and parts shorten it; at D=128 the
+    // softmax is the bound and the hand-offs only lengthen it (one part, -25 % with four).
+    static constexpr int P_PARTS = (D == 256) ? 4 : 1;
+    static_assert(P_PARTS == 1 || P_PARTS == 2 || P_PARTS == 4, "P hand-off parts");
     static constexpr int NBARS = 1 + 2 * NSLOTS + (1 + P_PARTS) * NSBUF + O_DONE_RING + 2;
     static constexpr int BAR_OFF = Q_BYTES + NSLOTS * HALF_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFF + BAR_AREA + 1024;
@@ -480,10 +484,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     exp_part(std::true_type{}, part);
                 else
                     exp_part(std::false_type{}, part);
-                if constexpr (PW == 16)
+                if constexpr (PW == 16) {
                     ptx::tmem_st16(ts + 16 * Q, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * Q]));
-                else
-                    ptx::tmem_st32(ts + 32 * Q, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * Q]));
+                } else {
+#pragma unroll
+                    for (int w = 0; w < PW; w += 32)
+                        ptx::tmem_st32(ts + PW * Q + w, *reinterpret_cast<uint32_t(*)[32]>(&pk[PW * Q + w]));
+                }
                 ptx::tmem_wait_st();
             };
             // One arrival per warp on the leader's barrier, after every lane's TMEM writes.
@@ -523,8 +530,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 ptx::tmem_wait_st();
             }
             hand_over(part_bar(0));
-            compute_part(std::integral_constant<int, 1>{});
-            hand_over(part_bar(1));
+            if constexpr (L::P_PARTS >= 2) {
+                compute_part(std::integral_constant<int, 1>{});
+                hand_over(part_bar(1));
+            }
             if constexpr (L::P_PARTS == 4) {
                 compute_part(std::integral_constant<int, 2>{});
                 hand_over(part_bar(2));
