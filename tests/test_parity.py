@@ -239,3 +239,25 @@ def test_large_scores_saturate_cleanly(dtype):
     assert st["nan_o"] == 0 and st["nan_lse"] == 0
     assert st["max_abs"] <= (2e-2 if dtype == "fp16" else 4e-2), st
     assert st["lse_max_abs"] <= 1e-6 * max(1.0, float(np.abs(ref_l).max())) * 8, st
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_peaky_keys_on_cta_pairs(dtype):
+    """1 % of the key rows scaled by 8 at D=256 with two heads per group and whole query tiles (CTA
+    pairs): a row's maximum jumps when a scaled key arrives in a later tile, so O is rescaled before
+    the first part of P is handed to the PV MMAs."""
+    check_full(Workload(f"peaky_pair_{dtype}", 1, 4, 2, 256, 2048, 256, dtype, seed=47, peaky_k=True))
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_large_scores_on_cta_pairs(dtype):
+    """The saturating case above at D=256 on CTA pairs (whole query tiles, two heads per group)."""
+    w = Workload(f"large_pair_{dtype}", 1, 4, 2, 256, 700, 256, dtype, seed=98)
+    q, k, v = workloads.make_inputs(w)
+    q, k = (q.float() * 24).to(q.dtype), (k.float() * 24).to(k.dtype)
+    o, lse = gpu_run(q, k, v, w.softmax_scale)
+    ref_o, ref_l = oracle.sdp_fwd(q, k, v, ORACLE_DTYPE[dtype], w.shape, w.softmax_scale)
+    st = compare(o, lse, ref_o, ref_l, dtype)
+    assert st["nan_o"] == 0 and st["nan_lse"] == 0
+    assert st["max_abs"] <= (2e-2 if dtype == "fp16" else 4e-2), st
+    assert st["lse_max_abs"] <= 1e-6 * max(1.0, float(np.abs(ref_l).max())) * 8, st
