@@ -315,6 +315,7 @@ int launch(const Shape &sh, const void *q, const void *k, const void *v, void *o
     p.kv_splits = sh.splits;
     p.tiles_per_split = sh.tiles_per_split;
     p.planes_q = static_cast<int>(sh.planes_q);
+    p.o = o;  // [planes, Sq, D]: the persistent CTA-pair kernel writes O rows directly
 
     const int grid = static_cast<int>(sh.units * sh.splits);
     cudaError_t e;

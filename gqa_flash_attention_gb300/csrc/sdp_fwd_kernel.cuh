@@ -55,6 +55,7 @@ enum : uint32_t {
 constexpr int DEBUG_NO_LOADS = 1;
 constexpr int DEBUG_SINGLE_CTA = 2;  // never use the CTA-pair kernel
 constexpr int DEBUG_PAIR_D128 = 8;   // use the CTA-pair kernel at D=128 too, where it qualifies
+constexpr int DEBUG_NO_PERSIST = 16; // one unit per CTA pair even where the persistent form applies
 constexpr int NUM_THREADS = 256;
 constexpr int O_DONE_RING = 4;  // PV completion barriers, used round robin
 

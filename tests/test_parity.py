@@ -261,3 +261,30 @@ def test_large_scores_on_cta_pairs(dtype):
     assert st["nan_o"] == 0 and st["nan_lse"] == 0
     assert st["max_abs"] <= (2e-2 if dtype == "fp16" else 4e-2), st
     assert st["lse_max_abs"] <= 1e-6 * max(1.0, float(np.abs(ref_l).max())) * 8, st
+
+
+DEBUG_NO_PERSIST = 16
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_persistent_pair_kernel_every_row(dtype):
+    """160 units (more than the SMs) of a dense, non-causal D=256 launch run on the persistent CTA-pair
+    kernel: each cluster takes several unit pairs, so tile counters, ring positions and barrier phases
+    carry over unit boundaries; the last KV tile is ragged."""
+    check_full(Workload(f"persist_{dtype}", 1, 8, 2, 2560, 700, 256, dtype, seed=48))
+
+
+def test_persistent_pair_kernel_matches_the_per_unit_launch_bit_for_bit():
+    """The persistent form changes the schedule, not the arithmetic: same O and LSE bits as one unit
+    pair per cluster."""
+    w = Workload("persist_eq", 1, 8, 2, 2560, 1000, 256, "fp16", seed=49)
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    o1, l1 = sdp.sdp_fwd(q, k, v)
+    assert sdp.poll_status() == sdp.SDP_OK
+    old = sdp.set_debug_flags(DEBUG_NO_PERSIST)
+    try:
+        o2, l2 = sdp.sdp_fwd(q, k, v)
+        assert sdp.poll_status() == sdp.SDP_OK
+    finally:
+        sdp.set_debug_flags(old)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

@@ -28,10 +28,13 @@ def _built():
     sdp.lib()
 
 
-@pytest.mark.parametrize("flags", [DEBUG_NO_LOADS, DEBUG_NO_LOADS | DEBUG_SINGLE_CTA],
-                         ids=["cta_pair", "single_cta"])
-def test_wait_timeout_is_reported_and_the_context_survives(flags):
-    w = Workload("timeout", 1, 4, 2, 256, 384, 128, "fp16", seed=91)  # two heads per group: CTA pairs
+@pytest.mark.parametrize("flags,w", [
+    (DEBUG_NO_LOADS, Workload("timeout", 1, 4, 2, 256, 384, 128, "fp16", seed=91)),  # two heads per group: CTA pairs
+    (DEBUG_NO_LOADS | DEBUG_SINGLE_CTA, Workload("timeout", 1, 4, 2, 256, 384, 128, "fp16", seed=91)),
+    # 160 units of a dense D=256 launch: the persistent CTA-pair kernel
+    (DEBUG_NO_LOADS, Workload("timeout_persist", 1, 8, 2, 2560, 384, 256, "fp16", seed=92)),
+], ids=["cta_pair", "single_cta", "persistent_pair"])
+def test_wait_timeout_is_reported_and_the_context_survives(flags, w):
     q, k, v = (t.cuda() for t in workloads.make_inputs(w))
     assert sdp.poll_status() == sdp.SDP_OK
     old_ms = sdp.set_wait_timeout_ms(50)
