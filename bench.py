@@ -304,7 +304,8 @@ def launch_shape(w):
 def kernel_name(w):
     """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
     the units of each (batch, KV head) pair up (and, causal, share the query
-    tile), else the single-CTA kernel; split-KV adds the merge kernel;
+    tile), in its persistent form for dense non-causal launches with more
+    units than SMs, else the single-CTA kernel; split-KV adds the merge kernel;
     variable-length batches pair up when the group size is even; head dim 128
     always runs on single CTAs."""
     if w.D == 128:
@@ -316,7 +317,14 @@ def kernel_name(w):
     n_qtiles = (sq + 127) // 128
     pair = (n_qtiles * G) % 2 == 0 and not (w.causal and G % 2)
     name = "sdp_fwd_pair_kernel" if pair else "sdp_fwd_kernel"
-    return name + " + merge_kernel" if w.kv_splits != 1 else name
+    if w.kv_splits != 1:
+        return name + " + merge_kernel"
+    # dense, non-causal CTA-pair launches with more units than SMs run the persistent form
+    units = w.B * w.Hkv * G * n_qtiles
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+    if pair and not w.causal and units > sms:
+        return "sdp_fwd_pair_persistent_kernel"
+    return name
 
 
 L2_BYTES = 126 * 2 ** 20
