@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -193,6 +194,15 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 namespace {
 
 constexpr int kDebugNoPack = 4;  // host-side test hook: never pack the query heads of a group
+// Host-side test hook: variable-length launches cover n_qtiles tiles for every sequence
+// instead of the compact list of the tiles that exist.
+constexpr int kDebugFullVarlenGrid = 32;
+// Sequences per batch up to which variable-length launches use the compact list. Each CTA
+// finds its tile by scanning the offsets, 32 sequences per step: one pass (stopping at its
+// sequence) without the causal mask; with it, one pass and a binary search over tile
+// levels on counts held in registers. These limits keep that under a microsecond or so.
+constexpr int kCompactMaxSeqs = 512;
+constexpr int kCompactMaxSeqsCausal = sdp::VARLEN_LEVEL_MAX_SEQS;
 
 int validate(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int Hq, int Hkv,
              int Sq, int Skv, int D, float scale, int dtype)
@@ -448,8 +458,16 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
     p.cu_k = cu_seqlens_k;
     p.o = o;
     p.o_row_stride = static_cast<long long>(Hq) * D;
+    // Valid sequences hold at most total_q rows in all, so the tiles that exist number at
+    // most (total_q + 127 * nseq) / 128: the compact grid has that many slots per head.
+    p.nseq = nseq;
+    const long long slots = std::min(static_cast<long long>(nseq) * n_qtiles,
+                                     (static_cast<long long>(total_q) + 127LL * nseq) / 128);
+    const bool compact = nseq <= (causal ? kCompactMaxSeqsCausal : kCompactMaxSeqs) &&
+                         !(p.debug_flags & kDebugFullVarlenGrid);
+    p.n_tiles = compact ? static_cast<int>(slots) : 0;
 
-    const int grid = static_cast<int>(units);
+    const int grid = static_cast<int>(compact ? slots * Hq : units);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (D == 128)
         e = dtype == SDP_BF16 ? sdp::launch_d128_bf16(maps, p, grid, st) : sdp::launch_d128_fp16(maps, p, grid, st);

@@ -187,6 +187,142 @@ __device__ __forceinline__ SeqGeom seq_geom(const KernelParams &p, int b)
     return SeqGeom{q0, k0, q1 - q0, k1 - k0, ok};
 }
 
+// What the compact unit list of a variable-length batch reads (by value, so the
+// scan below takes no pointer to the kernel's parameters).
+struct VarlenScan {
+    const int *cu_q, *cu_k;
+    int nseq, n_qtiles, Sq, Skv;
+};
+struct TileRef {
+    int b, qt;
+    bool found, any_bad;
+};
+
+// Query tiles of sequence idx: ceil(rows / 128), or 0 for an index past the
+// batch or a sequence whose offsets fail seq_geom's checks (then `bad` is set).
+__device__ __forceinline__ int varlen_tiles(const VarlenScan &v, int idx, bool &bad)
+{
+    bad = false;
+    if (idx >= v.nseq)
+        return 0;
+    const int q0 = __ldg(v.cu_q + idx), q1 = __ldg(v.cu_q + idx + 1);
+    const int k0 = __ldg(v.cu_k + idx), k1 = __ldg(v.cu_k + idx + 1);
+    const bool ok = 0 <= q0 && q0 <= q1 && q1 <= v.Sq && 0 <= k0 && k0 <= k1 && k1 <= v.Skv &&
+                    q1 - q0 <= v.n_qtiles * 128;
+    bad = !ok;
+    return ok ? (q1 - q0 + 127) / 128 : 0;
+}
+
+// The compact unit list of a variable-length batch (p.n_tiles > 0) holds only
+// the query tiles that exist, sum over sequences of ceil(rows / 128), instead of
+// the longest sequence's tile count for every sequence. Entry t of the list, in
+// sequence order then tile order, or (by_level, causal launches) in descending
+// tile index then sequence order, so that the units that read the most KV tiles
+// start first. Computed by every warp on its own (lanes take 32 sequences at a
+// time; no shared memory, no barrier); `found` is false past the last real
+// tile. any_bad reports a sequence with invalid offsets among those scanned:
+// all of them when scan_all or by_level, else those up to the one found.
+static __device__ __noinline__ TileRef varlen_tile(const VarlenScan v, int t, bool by_level, bool scan_all)
+{
+    constexpr unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    TileRef r{0, 0, false, false};
+    if (!by_level) {
+        int acc = 0;  // tiles of the sequences before this group of 32
+        for (int base = 0; base < v.nseq; base += 32) {
+            bool bad;
+            const int nb = varlen_tiles(v, base + lane, bad);
+            r.any_bad |= __any_sync(FULL, bad);
+            int incl = nb;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int x = __shfl_up_sync(FULL, incl, d);
+                if (lane >= d)
+                    incl += x;
+            }
+            const int excl = incl - nb;
+            const unsigned hit = __ballot_sync(FULL, acc + excl <= t && t < acc + incl);
+            if (hit != 0u) {
+                const int src = __ffs(hit) - 1;
+                r.b = base + src;
+                r.qt = t - acc - __shfl_sync(FULL, excl, src);
+                r.found = true;
+            }
+            acc += __shfl_sync(FULL, incl, 31);
+            if (r.found && !scan_all)
+                break;
+        }
+        return r;
+    }
+    // Level order, for at most VARLEN_LEVEL_MAX_SEQS = 64 sequences (the host's limit for
+    // it): two tile counts per lane, held in registers. Tiles with index >= q number
+    // C(q) = sum_b max(0, n_b - q); entry t lies on the level q with C(q + 1) <= t < C(q).
+    static_assert(VARLEN_LEVEL_MAX_SEQS <= 64, "two sequences per lane");
+    bool bad0, bad1;
+    const int n0 = varlen_tiles(v, lane, bad0);
+    const int n1 = varlen_tiles(v, lane + 32, bad1);
+    r.any_bad = __any_sync(FULL, bad0 || bad1);
+    auto count_from = [&](int q) -> int {
+        int s = max(0, n0 - q) + max(0, n1 - q);
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1)
+            s += __shfl_xor_sync(FULL, s, d);
+        return s;
+    };
+    if (t >= count_from(0))
+        return r;
+    int lo = 0, hi = v.n_qtiles - 1;  // the largest q with C(q) > t
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (count_from(mid) > t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    int rank = t - count_from(lo + 1);  // among the sequences with more than lo tiles
+    unsigned m = __ballot_sync(FULL, n0 > lo);
+    const unsigned m1 = __ballot_sync(FULL, n1 > lo);
+    int base = 0;
+    if (rank >= __popc(m)) {
+        rank -= __popc(m);
+        m = m1;
+        base = 32;
+    }
+    for (int i = 0; i < rank; ++i)
+        m &= m - 1u;
+    r.b = base + __ffs(m) - 1;
+    r.qt = lo;
+    r.found = true;
+    return r;
+}
+
+// Slot u (head-in-group index already taken out) of a compact variable-length
+// launch, n_tiles slots per KV head. Without the causal mask a KV head's tiles
+// run sequence by sequence (their K/V stay in L2); with it, in level order
+// across the KV heads. Block 0 scans every sequence and reports invalid offsets.
+// Returns the unit index that the full grid gives the same (sequence, tile, KV
+// head), so that one decode serves both grids, or -1 for a slot past the last
+// real tile (both CTAs of a pair get the same answer).
+__device__ __forceinline__ int varlen_compact_unit(const KernelParams &p, int u)
+{
+    int t, g;
+    if (p.causal) {
+        g = u % p.Hkv;
+        t = u / p.Hkv;
+    } else {
+        t = u % p.n_tiles;
+        g = u / p.n_tiles;
+    }
+    const TileRef r = varlen_tile(VarlenScan{p.cu_q, p.cu_k, p.nseq, p.n_qtiles, p.Sq, p.Skv}, t, p.causal != 0,
+                                  blockIdx.x == 0);
+    if (r.any_bad && blockIdx.x == 0 && threadIdx.x == 0)
+        atomicCAS(p.status, 0u, static_cast<unsigned>(SITE_SEQLENS));
+    if (!r.found)
+        return -1;
+    const int bg = r.b * p.Hkv + g;
+    return p.causal ? (p.n_qtiles - 1 - r.qt) * (p.nseq * p.Hkv) + bg : bg * p.n_qtiles + r.qt;
+}
+
 // Position of a chunk in the load order K_0, then for j = 0..n-1: K_{j+1} (if
 // any), V_j. Tiles are CPT chunks long; the producer and both issuers derive
 // ring slot = pos % NSLOTS and phase = (pos / NSLOTS) & 1 from it. Every
@@ -203,7 +339,9 @@ __device__ __forceinline__ int pos_v(int j, int n)
     return j == n - 1 ? CPT * (2 * j + 1) : CPT * (2 * j + 2);
 }
 
-template <int D, bool BF16>
+// VARLEN: launched for variable-length batches (p.cu_q != nullptr); only that
+// instantiation carries the compact unit list's decode.
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     sdp_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -246,13 +384,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     u -= split * units_per_split;
     const int hi = u % p.G;
     u /= p.G;
+    if constexpr (VARLEN) {
+        if (p.n_tiles > 0 && (u = varlen_compact_unit(p, u)) < 0)
+            return;  // a slot past the last query tile
+    }
     int qt, bg;  // query tile; b * Hkv + g
     if (p.cu_q != nullptr && p.causal) {
         // Causal variable-length batch: query tile outermost, highest first. A unit of tile qt
-        // reads qt + 1 KV tiles whatever its sequence, so the costliest units start first and the
-        // tiles past shorter sequences (which return at once) come last. (Without the mask a
-        // unit's cost is its sequence's key count, unrelated to qt: the group-major order stays.)
-        const int n_bg = units_per_split / (p.G * p.n_qtiles);
+        // reads qt + 1 KV tiles whatever its sequence, so the costliest units start first.
+        // (Without the mask a unit's cost is its sequence's key count, unrelated to qt: the
+        // group-major order stays.)
+        const int n_bg = VARLEN ? p.nseq * p.Hkv : units_per_split / (p.G * p.n_qtiles);
         qt = p.n_qtiles - 1 - u / n_bg;
         bg = u % n_bg;
     } else {
@@ -694,7 +836,7 @@ template <int D, bool BF16>
 cudaError_t launch_sdp_fwd(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o,
                            const KernelParams &p, int grid, cudaStream_t stream)
 {
-    auto kern = sdp_fwd_kernel<D, BF16>;
+    auto kern = p.cu_q != nullptr ? sdp_fwd_kernel<D, BF16, true> : sdp_fwd_kernel<D, BF16, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::SMEM_BYTES);
     if (e != cudaSuccess)
         return e;

@@ -106,7 +106,7 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t pari
     return wait_slow_cluster(bar, parity, cx.abort_flag, cx.status, cx.timeout_ns, site);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     sdp_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -150,13 +150,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     u -= split * units_per_split;
     const int hi = u % p.G;
     u /= p.G;
+    if constexpr (VARLEN) {
+        if (p.n_tiles > 0 && (u = varlen_compact_unit(p, u)) < 0)
+            return;  // both CTAs of the pair: the same slot past the last query tile
+    }
     int qt, bg;  // query tile; b * Hkv + g
     if (p.cu_q != nullptr && p.causal) {
         // Causal variable-length batch: query tile outermost, highest first. A unit of tile qt
-        // reads qt + 1 KV tiles whatever its sequence, so the costliest units start first and the
-        // tiles past shorter sequences (which return at once) come last. (Without the mask a
-        // unit's cost is its sequence's key count, unrelated to qt: the group-major order stays.)
-        const int n_bg = units_per_split / (p.G * p.n_qtiles);
+        // reads qt + 1 KV tiles whatever its sequence, so the costliest units start first.
+        // (Without the mask a unit's cost is its sequence's key count, unrelated to qt: the
+        // group-major order stays.)
+        const int n_bg = VARLEN ? p.nseq * p.Hkv : units_per_split / (p.G * p.n_qtiles);
         qt = p.n_qtiles - 1 - u / n_bg;
         bg = u % n_bg;
     } else {
@@ -648,7 +652,7 @@ template <int D, bool BF16>
 cudaError_t launch_sdp_fwd_pair(const CUtensorMap &q, const CUtensorMap &k_half, const CUtensorMap &v,
                                 const CUtensorMap &o, const KernelParams &p, int grid, cudaStream_t stream)
 {
-    auto kern = sdp_fwd_pair_kernel<D, BF16>;
+    auto kern = p.cu_q != nullptr ? sdp_fwd_pair_kernel<D, BF16, true> : sdp_fwd_pair_kernel<D, BF16, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairLayout<D>::SMEM_BYTES);
     if (e != cudaSuccess)

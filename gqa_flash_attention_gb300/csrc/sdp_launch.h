@@ -30,7 +30,16 @@ struct KernelParams {
     const int *cu_q, *cu_k;
     void *o;
     long long o_row_stride;
+    // Compact unit list of a variable-length batch (n_tiles > 0): n_tiles list
+    // slots per query head, at least the number of query tiles that exist
+    // (sum over the nseq sequences of ceil(rows / 128)); slots past the last
+    // real tile return at once. 0: the grid covers n_qtiles tiles per sequence.
+    int nseq, n_tiles;
 };
+
+// Sequences per batch up to which causal variable-length launches use the compact
+// unit list (its level-order search holds two sequences per lane in registers).
+constexpr int VARLEN_LEVEL_MAX_SEQS = 64;
 
 // Tensor maps of one launch: Q, K, V, O with 128-row boxes, and K with 64-row
 // boxes (half a KV tile) for the CTA-pair kernel.

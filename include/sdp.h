@@ -156,15 +156,20 @@ int sdp_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float 
  * o       device, [total_q, Hq, D] (written); lse [Hq, total_q] fp32 or NULL
  * cu_seqlens_q, cu_seqlens_k  device int32 [nseq + 1]: 0, then non-decreasing
  *         offsets, ending at total_q / total_k
- * max_seqlen_q  host int >= every query length (it sizes the grid: 128-row
- *         tiles of the longest sequence per (sequence, head))
+ * max_seqlen_q  host int >= every query length. Up to 512 sequences (64 with
+ *         causal != 0) the grid holds only the 128-row tiles that exist, at
+ *         most (total_q + 127 * nseq) / 128 per head, and each CTA finds its
+ *         tile from the offsets; beyond that it holds the longest sequence's
+ *         tiles for every (sequence, head)
  * Hq % Hkv == 0, D in {128, 256}; total_q == 0 returns SDP_OK at once (null
  * pointers allowed then), before the other checks.
  *
  * Ownership and aliasing as sdp_fwd. The offsets live on the device, so they
  * are checked by the kernel: a sequence whose offsets leave [0, total], go
  * down, or give more rows than max_seqlen_q rounded up to a multiple of 128
- * is not computed, and the next sdp_poll_status returns SDP_ERR_BAD_SEQLENS. Inputs must be finite: the key rows after a
+ * is not computed (nor, where offsets that go down make sequences overlap,
+ * those past the grid's tile count), and the next sdp_poll_status returns
+ * SDP_ERR_BAD_SEQLENS. Inputs must be finite: the key rows after a
  * sequence's last key in its last 128-key tile belong to the next sequence
  * and are read, with weight exactly 0. With an even number of query heads per
  * KV head, tiles run on CTA pairs (two heads of a group on one tile); tiles
@@ -243,7 +248,11 @@ unsigned int sdp_set_wait_timeout_ms(unsigned int ms);
  * the same result; tests compare them). Bit 2: never pack the query heads of
  * a group into one head (same result; tests compare). Bit 3: at head dim 128,
  * use the CTA-pair kernel where it qualifies (by default head dim 128 runs on
- * single CTAs, which measured as fast or faster there). Returns the previous flags.
+ * single CTAs, which measured as fast or faster there). Bit 4: one CTA pair
+ * per unit even where the persistent CTA-pair kernel applies (same result, bit
+ * for bit). Bit 5: variable-length launches cover the longest sequence's query
+ * tiles for every sequence instead of the list of tiles that exist (same
+ * result, bit for bit). Returns the previous flags.
  */
 int sdp_set_debug_flags(int flags);
 

@@ -22,6 +22,7 @@ pytestmark = pytest.mark.gpu
 
 DEBUG_SINGLE_CTA = 2
 DEBUG_PAIR_D128 = 8
+DEBUG_FULL_VARLEN_GRID = 32
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -121,7 +122,16 @@ def test_one_sequence_equals_the_dense_call(causal):
     assert torch.equal(lse, ld[0])
 
 
-def test_bad_offsets_are_reported_and_skipped():
+@pytest.mark.parametrize("flags", [0, DEBUG_FULL_VARLEN_GRID], ids=["compact_grid", "full_grid"])
+def test_bad_offsets_are_reported_and_skipped(flags):
+    old = sdp.set_debug_flags(flags)
+    try:
+        _bad_offsets()
+    finally:
+        sdp.set_debug_flags(old)
+
+
+def _bad_offsets():
     dev = torch.device("cuda")
     w = VarlenWorkload("bad", (100, 200), (100, 200), 4, 1, 128, "fp16", seed=88)
     q, k, v = (t.to(dev) for t in workloads.make_varlen_inputs(w))
@@ -140,6 +150,43 @@ def test_bad_offsets_are_reported_and_skipped():
     # the status word was cleared: a good call afterwards reports OK
     sdp.sdp_fwd_varlen(q, k, v, good_q, good_k, 200)
     assert sdp.poll_status() == sdp.SDP_OK
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_compact_grid_matches_the_full_grid_bit_for_bit(w):
+    """The compact grid (only the query tiles that exist, each CTA finding its
+    tile from the offsets) and the full grid (the longest sequence's tiles for
+    every sequence) run the same per-tile arithmetic: identical outputs."""
+    q, k, v = workloads.make_varlen_inputs(w)
+    o, lse = run(w, q, k, v)
+    old = sdp.set_debug_flags(DEBUG_FULL_VARLEN_GRID)
+    try:
+        of, lf = run(w, q, k, v)
+    finally:
+        sdp.set_debug_flags(old)
+    assert torch.equal(o, of)
+    assert torch.equal(lse, lf)
+
+
+def _many(n, causal, seed):
+    rng = np.random.default_rng(seed)
+    lq = tuple(int(x) for x in rng.integers(0, 300, size=n))
+    lk = tuple(int(x) for x in rng.integers(0, 300, size=n))
+    return VarlenWorkload(f"many{n}_{'causal' if causal else 'full'}", lq, lk, 4, 2, 128, "bf16", seed=seed,
+                          causal=causal)
+
+
+# Sequence counts on both sides of the limits up to which the compact grid is used
+# (512 sequences without the causal mask, 64 with it), plus one long sequence after
+# many short ones.
+MANY = [_many(64, True, 91), _many(65, True, 92), _many(100, False, 93), _many(513, False, 94),
+        VarlenWorkload("short_then_long", (1,) * 40 + (1000,), (1,) * 40 + (1000,), 4, 1, 256, "fp16", seed=95,
+                       causal=True)]
+
+
+@pytest.mark.parametrize("w", MANY, ids=lambda w: w.name)
+def test_many_sequences_every_row(w):
+    check_every_row(w)
 
 
 def test_zero_query_rows_is_a_no_op():
