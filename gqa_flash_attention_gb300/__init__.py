@@ -315,6 +315,15 @@ def set_wait_timeout_ms(ms: int) -> int:
 
 
 def set_debug_flags(flags: int) -> int:
+    """Test hooks of the C library (0 by default; returns the previous flags).
+
+    1: the load warp issues no copies (every wait runs out: the timeout path);
+    2: never the CTA-pair kernel; 4: never pack a group's query heads; 8: the
+    CTA-pair kernel at head dim 128 too; 16: one CTA pair per unit where the
+    persistent kernel would run; 32: variable-length launches on the full grid
+    instead of the compact tile list. 4, 16 and 32 give bit-identical results;
+    2 and 8 switch kernels that compute the same function.
+    """
     return int(lib().sdp_set_debug_flags(int(flags)))
 
 
