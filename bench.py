@@ -49,8 +49,10 @@ def parse():
     ap.add_argument("--cpu-rows", type=int, default=0, help="query rows per head in the CPU sample (0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["attention", "merge"], default="attention",
-                    help="merge: time sdp_merge (HBM-bound) on a context-parallel-shaped case instead")
+    ap.add_argument("--op", choices=["attention", "merge", "host"], default="attention",
+                    help="merge: time sdp_merge (HBM-bound) on a context-parallel-shaped case instead; host: "
+                         "the host time of one sdp_fwd call (argument checks, tensor maps, launch) on the "
+                         "smallest workload")
     ap.add_argument("--merge-parts", type=int, default=8)
     ap.add_argument("--override", nargs="*", default=[], metavar="FIELD=VALUE",
                     help="change fields of a dense workload (B, Hq, Hkv, Sq, Skv): a smaller case of the same "
@@ -147,8 +149,79 @@ def load_traffic(workload: str, prefix: str = "sdp_fwd_", current_hash=None):
         return None
 
 
+class NvmlSampler:
+    """Read-only NVML queries (SM clock, power, clock-event reasons) every ~10 ms in a
+    background thread while the timed region runs, through ctypes on the driver's
+    libnvidia-ml (no Python package needed). Nothing is set or reset."""
+
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        import ctypes
+        self.period = period_s
+        self.rows = []
+        self.thread = None
+        self.stop_flag = False
+        self.ok = False
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(h)) != 0:
+                return
+            self.nv, self.h, self.ct = nv, h, ctypes
+            mx = ctypes.c_uint()
+            self.sm_max = float(mx.value) if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+            self.ok = self.sample() is not None
+        except Exception:
+            self.ok = False
+
+    def sample(self):
+        ct, nv, h = self.ct, self.nv, self.h
+        clk, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) != 0:  # NVML_CLOCK_SM
+            return None
+        power = mw.value / 1000.0 if nv.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else None
+        reasons = rs.value if self.reasons_fn is not None and self.reasons_fn(h, ct.byref(rs)) == 0 else 0
+        return float(clk.value), power, reasons
+
+    def _loop(self):
+        while not self.stop_flag:
+            r = self.sample()
+            if r is not None:
+                self.rows.append(r)
+            time.sleep(self.period)
+
+    def start(self):
+        import threading
+        self.rows = []
+        self.stop_flag = False
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag = True
+        self.thread.join(timeout=5)
+        r = self.sample()  # at least one reading from the end of the region
+        if r is not None:
+            self.rows.append(r)
+        sm = [x[0] for x in self.rows]
+        pw = [x[1] for x in self.rows if x[1] is not None]
+        reasons = sorted({name for x in self.rows for bit, name in self.REASONS.items() if x[2] & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_mhz_min": min(sm) if sm else None,
+                "sm_max_mhz": self.sm_max, "power_w_max": max(pw) if pw else None,
+                "power_w_median": statistics.median(pw) if pw else None, "samples": len(sm),
+                "period_ms": 1000 * self.period, "source": "NVML (read-only), in-process", "reasons": reasons}
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    """nvidia-smi clock / throttle-reason samples while the timed region runs (the
+    fallback where NVML cannot be loaded in-process)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -164,7 +237,7 @@ class ClockSampler:
             pass
 
     def start(self):
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
         if self.uuid:
             cmd += ["-i", self.uuid]
         try:
@@ -202,6 +275,20 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "power_w_max": max(pw) if pw else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def clock_sampler(device_index: int):
+    """NVML sampling every 10 ms where it loads, else nvidia-smi every 50 ms."""
+    nv = NvmlSampler(device_index)
+    return nv if nv.ok else ClockSampler(device_index)
+
+
+# The second roofline denominator: NVIDIA's nominal dense fp16/bf16 tensor rate of one
+# GB300 (HGX B300 specifications: 36 PFLOPS FP16/BF16 per 8 GPUs, quoted with 2:4
+# sparsity; dense is half of that, per GPU 2.25 PFLOPS).
+DATASHEET_TFLOPS = 2250.0
+DATASHEET_SOURCE = ("NVIDIA HGX B300 specifications: 36 PFLOPS FP16/BF16 per 8 GPUs with 2:4 sparsity "
+                    "= 2.25 PFLOPS dense per GPU")
 
 
 def is_varlen(w):
@@ -283,13 +370,19 @@ def reference_arm(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.median(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_of(w, args.gpus),
+        "data": "synthetic", "config": {**config_of(w, args.gpus), "cuda_graph": use_graph_for(args, w)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
                          "extrapolated_full_workload_s": w.flops() / (value * 1e12)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
+
+
+def use_graph_for(args, w):
+    """Whether our arm replays each step from a CUDA graph (auto: the split-KV decode
+    workloads, whose steps are shorter than the host's per-call work)."""
+    return args.graph == "on" or (args.graph == "auto" and not is_varlen(w) and w.kv_splits != 1)
 
 
 def launch_shape(w):
@@ -399,7 +492,7 @@ def ours_arm(args, w):
     torch.cuda.synchronize(dev)
     if sdp.poll_status() != sdp.SDP_OK:
         raise RuntimeError("kernel reported a timeout during warm-up")
-    use_graph = args.graph == "on" or (args.graph == "auto" and not is_varlen(w) and w.kv_splits != 1)
+    use_graph = use_graph_for(args, w)
     step = call
     if use_graph:
         graph = torch.cuda.CUDAGraph()
@@ -412,7 +505,7 @@ def ours_arm(args, w):
     K = args.steps
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    clocks = ClockSampler(dev.index)
+    clocks = clock_sampler(dev.index)
     clocks.start()
     if world > 1:
         torch.distributed.barrier()
@@ -527,6 +620,14 @@ def ours_arm(args, w):
                     "algorithmic_bytes": w.hbm_bytes(), "tflops": tflops}
     roofline.update({"kernel": kernel_name(w), "launch_ms_median": statistics.median(per_launch_ms),
                      "flop_per_byte": intensity})
+    if roofline["bound"] == "tensor":
+        roofline.update({"peak_datasheet": DATASHEET_TFLOPS, "frac_datasheet": tflops / DATASHEET_TFLOPS,
+                         "peak_datasheet_source": DATASHEET_SOURCE})
+    # FLOP per SM per clock at the sampled median SM clock: comparable across power states
+    # (the tensor cores' nominal dense fp16/bf16 rate is 8192 per SM per clock)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if clk.get("sm_mhz"):
+        roofline["flop_per_sm_cycle"] = w.flops() / (avg_launch_ms * 1e-3 * clk["sm_mhz"] * 1e6 * sms)
     achieved = tflops
 
     cpu = None
@@ -541,8 +642,8 @@ def ours_arm(args, w):
     cfg["cuda_graph"] = use_graph
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic", "config": cfg,
+        "ms_per_step": ms_per_step, "latency_us_per_step": 1000 * ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
         "gpu_launches": K * launches_per_step,
@@ -567,7 +668,7 @@ def merge_arm(args, w):
         sdp.sdp_merge(o_parts, lse_parts, out=o, lse=lse)
     K = args.steps
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
-    clocks = ClockSampler(0)
+    clocks = clock_sampler(0)
     clocks.start()
     torch.cuda.synchronize(dev)
     ev[0].record()
@@ -592,6 +693,49 @@ def merge_arm(args, w):
         "clocks": clk, "gpu_launches": K}), flush=True)
 
 
+def host_arm(args):
+    """Host-side cost of one call: back-to-back sdp_fwd calls on gqa4_s256_d128_fp16
+    (whose kernel is shorter than the call, so the launch queue never fills), timed with
+    the host clock; the ctypes cost of a trivial exported call is reported beside it."""
+    import ctypes
+    import gqa_flash_attention_gb300 as sdp
+    w = workloads.ALL_WORKLOADS["gqa4_s256_d128_fp16"]
+    dev = torch.device("cuda", 0)
+    q, k, v = (t.to(dev) for t in workloads.make_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream(dev).cuda_stream
+    args_ptr = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.Hq, w.Hkv, w.Sq,
+                w.Skv, w.D, w.softmax_scale, sdp.SDP_FP16, st)
+    L = sdp.lib()
+    raw = L.sdp_fwd
+    c_args = [ctypes.c_void_p(a) for a in args_ptr[:5]] + list(args_ptr[5:11]) + \
+        [ctypes.c_float(args_ptr[11]), args_ptr[12], ctypes.c_void_p(st)]
+    n = max(args.steps, 200)
+
+    def per_call_us(fn):
+        for _ in range(args.warmup + 10):
+            fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize(dev)
+        return 1e6 * (t1 - t0) / n
+
+    res = {
+        "ctypes_trivial_call_us": per_call_us(lambda: L.sdp_version()),
+        "c_abi_call_us": per_call_us(lambda: raw(*c_args)),
+        "python_binding_call_us": per_call_us(lambda: sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse)),
+    }
+    if sdp.poll_status() != sdp.SDP_OK:
+        raise RuntimeError("kernel reported a timeout")
+    print(json.dumps({"metric": "host microseconds per sdp_fwd call", "value": res["c_abi_call_us"],
+                      "unit": "us", "higher_is_better": False, "steps": n, "warmup": args.warmup,
+                      "config": {"workload": w.name, "calls": n}, **res}), flush=True)
+
+
 def main():
     args = parse()
     w = BENCH_WORKLOADS[args.workload]
@@ -605,7 +749,9 @@ def main():
                 raise SystemExit(f"cannot override {key!r}")
             kw[key] = int(val)
         w = w.with_(name=w.name + "_" + "_".join(f"{k}{v}" for k, v in kw.items()), **kw)
-    if args.op == "merge":
+    if args.op == "host":
+        host_arm(args)
+    elif args.op == "merge":
         merge_arm(args, w)
     elif args.impl == "reference":
         reference_arm(args, w)

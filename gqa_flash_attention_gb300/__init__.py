@@ -331,15 +331,16 @@ def sdp_fwd_noalloc_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: in
                         D: int, scale: float, dtype: int, stream: int = 0) -> int:
     """The C call sdp_fwd_noalloc with integer addresses; returns the status code.
 
-    Same operation and arguments as sdp_fwd_ptr, but the library allocates no
-    device memory for it: for callers whose device memory is owned entirely by
-    their own pool or host application and that therefore cannot let a library
-    call cudaMalloc. Its status word lives in a 256-byte array inside the
-    library shared by all such calls, so overlapping calls on different
-    unordered streams race on it, and its timeouts are not reported by
-    poll_status().
+    Same operation, arguments and launch as sdp_fwd_ptr (bit-identical
+    outputs), but the library allocates no device memory for it: for callers
+    whose device memory is owned entirely by their own pool or host
+    application and that therefore cannot let a library call cudaMalloc. Its
+    status word lives in a 256-byte array inside the library shared by all
+    such calls, so overlapping calls on different unordered streams race on
+    it; read it with noalloc_status(), not poll_status().
     """
-    fn = lib().sdp_fwd_noalloc
+    L = lib()
+    fn = L.sdp_fwd_noalloc
     if fn.restype is not ctypes.c_int or fn.argtypes is None:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         fn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
@@ -347,6 +348,17 @@ def sdp_fwd_noalloc_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: in
     return int(fn(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.c_void_p(o),
                   ctypes.c_void_p(lse), int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(D), ctypes.c_float(scale),
                   int(dtype), ctypes.c_void_p(stream)))
+
+
+def noalloc_status(stream=None, device=None) -> int:
+    """Synchronise the stream, then read and clear sdp_fwd_noalloc's status word (allocates nothing)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    fn = lib().sdp_fwd_noalloc_status
+    if fn.restype is not ctypes.c_int or fn.argtypes is None:
+        fn.argtypes = [ctypes.c_void_p]
+        fn.restype = ctypes.c_int
+    with torch.cuda.device(dev):
+        return int(fn(ctypes.c_void_p(_stream_handle(stream, dev))))
 
 
 # Short names of the main entry points.

@@ -51,23 +51,48 @@ EncodeTiledFn encoder()
     return g_encode;
 }
 
-// Status word of `dev`, allocated (and zeroed) on first use.
-int device_state(int dev, unsigned int **status)
+// Facts of device `dev` that every launch needs, looked up once per device:
+// whether it is an sm_103 part, and its SM count.
+int g_sms[kMaxDevices] = {};
+
+int device_info_locked(int dev, int *sms)
 {
-    if (dev < 0 || dev >= kMaxDevices)
-        return SDP_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lk(g_mu);
     if (g_cc_checked[dev] == 0) {
-        int major = 0, minor = 0;
+        int major = 0, minor = 0, n = 0;
         cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         if (e == cudaSuccess)
             e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess)
             return cuda_fail(e);
+        g_sms[dev] = n;
         g_cc_checked[dev] = (major == 10 && minor == 3) ? 1 : -1;
     }
     if (g_cc_checked[dev] != 1)
         return SDP_ERR_UNSUPPORTED;
+    *sms = g_sms[dev];
+    return SDP_OK;
+}
+
+int device_info(int dev, int *sms)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return SDP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return device_info_locked(dev, sms);
+}
+
+// Status word of `dev`, allocated (and zeroed) on first use.
+int device_state(int dev, unsigned int **status, cudaStream_t)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return SDP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    int sms = 0;
+    int rc = device_info_locked(dev, &sms);
+    if (rc != SDP_OK)
+        return rc;
     if (g_status[dev] == nullptr) {
         unsigned int *p = nullptr;
         cudaError_t e = cudaMalloc(&p, sizeof(unsigned int));
@@ -287,16 +312,10 @@ long long workspace_bytes(const Shape &sh, int D)
     return align256(sh.splits * rows * D * 2) + sh.splits * rows * 4;
 }
 
-int sm_count(int dev, int *sms)
-{
-    cudaError_t e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
-    return e == cudaSuccess ? SDP_OK : cuda_fail(e);
-}
-
 // Encode the maps and launch the kernel for `sh`. O / LSE go to `o` / `lse`
 // ([splits * planes_q, Sq, D] and [splits * planes_q, Sq] when splits > 1).
 int launch(const Shape &sh, const void *q, const void *k, const void *v, void *o, float *lse, int Hkv, int Skv,
-           int D, float scale, int dtype, int causal, unsigned int *status, cudaStream_t st)
+           int D, float scale, int dtype, int causal, unsigned int *status, int sms, cudaStream_t st)
 {
     sdp::LaunchMaps maps;
     int rc;
@@ -326,6 +345,7 @@ int launch(const Shape &sh, const void *q, const void *k, const void *v, void *o
     p.tiles_per_split = sh.tiles_per_split;
     p.planes_q = static_cast<int>(sh.planes_q);
     p.o = o;  // [planes, Sq, D]: the persistent CTA-pair kernel writes O rows directly
+    p.num_sms = sms;
 
     const int grid = static_cast<int>(sh.units * sh.splits);
     cudaError_t e;
@@ -339,21 +359,7 @@ int launch(const Shape &sh, const void *q, const void *k, const void *v, void *o
 int forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
             int Skv, int D, float scale, int dtype, int causal, void *stream)
 {
-    // validation: no CUDA call happens before all of it passes
-    int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, dtype);
-    if (rc != SDP_OK)
-        return rc;
-    Shape sh;
-    if ((rc = shape_of(B, Hq, Hkv, Sq, Skv, causal, &sh)) != SDP_OK)
-        return rc;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return cuda_fail(e);
-    unsigned int *status = nullptr;
-    if ((rc = device_state(dev, &status)) != SDP_OK)
-        return rc;
-    return launch(sh, q, k, v, o, lse, Hkv, Skv, D, scale, dtype, causal, status, static_cast<cudaStream_t>(stream));
+    return sdp::forward_with(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, dtype, causal, device_state, stream);
 }
 
 // Shape of a split-KV call on the current device (validation of the sizes only).
@@ -372,12 +378,46 @@ int splitkv_shape(int B, int Hq, int Hkv, int Sq, int Skv, int D, int dtype, int
     if (e != cudaSuccess)
         return cuda_fail(e);
     int sms = 0;
-    if ((rc = sm_count(*dev, &sms)) != SDP_OK)
+    if ((rc = device_info(*dev, &sms)) != SDP_OK)
         return rc;
     return set_splits(sh, n_splits, sms);
 }
 
 }  // namespace
+
+namespace sdp {
+
+int forward_with(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
+                 int Skv, int D, float scale, int dtype, int causal, StatusSource status_of, void *stream)
+{
+    // validation: no CUDA call happens before all of it passes
+    int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, dtype);
+    if (rc != SDP_OK)
+        return rc;
+    Shape sh;
+    if ((rc = shape_of(B, Hq, Hkv, Sq, Skv, causal, &sh)) != SDP_OK)
+        return rc;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    int sms = 0;
+    if ((rc = device_info(dev, &sms)) != SDP_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int *status = nullptr;
+    if ((rc = status_of(dev, &status, st)) != SDP_OK)
+        return rc;
+    return launch(sh, q, k, v, o, lse, Hkv, Skv, D, scale, dtype, causal, status, sms, st);
+}
+
+int status_code_of(unsigned int word)
+{
+    g_last_detail.store(word);
+    return (word & 0xffu) == 7u ? SDP_ERR_BAD_SEQLENS : SDP_ERR_DEVICE_TIMEOUT;
+}
+
+}  // namespace sdp
 
 extern "C" {
 
@@ -423,9 +463,12 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return cuda_fail(e);
-    unsigned int *status = nullptr;
-    int rc = device_state(dev, &status);
+    int sms = 0;
+    int rc = device_info(dev, &sms);
     if (rc != SDP_OK)
+        return rc;
+    unsigned int *status = nullptr;
+    if ((rc = device_state(dev, &status, static_cast<cudaStream_t>(stream))) != SDP_OK)
         return rc;
     // A batch without keys still gets valid maps (one row); no load is issued then.
     const long long kv_rows = total_k > 0 ? total_k : 1;
@@ -458,6 +501,7 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
     p.cu_k = cu_seqlens_k;
     p.o = o;
     p.o_row_stride = static_cast<long long>(Hq) * D;
+    p.num_sms = sms;
     // Valid sequences hold at most total_q rows in all, so the tiles that exist number at
     // most (total_q + 127 * nseq) / 128: the compact grid has that many slots per head.
     p.nseq = nseq;
@@ -517,16 +561,19 @@ int sdp_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float 
             if (static_cast<const char *>(x) >= w0 && static_cast<const char *>(x) < w1)
                 return SDP_ERR_INVALID_ARG;
     }
-    unsigned int *status = nullptr;
-    if ((rc = device_state(dev, &status)) != SDP_OK)
-        return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int *status = nullptr;
+    if ((rc = device_state(dev, &status, st)) != SDP_OK)
+        return rc;
+    int sms = 0;
+    if ((rc = device_info(dev, &sms)) != SDP_OK)
+        return rc;
     if (sh.splits == 1)
-        return launch(sh, q, k, v, o, lse, Hkv, Skv, D, scale, dtype, 0, status, st);
+        return launch(sh, q, k, v, o, lse, Hkv, Skv, D, scale, dtype, 0, status, sms, st);
     const long long rows = sh.planes_q * sh.Sq;
     char *ws_o = static_cast<char *>(workspace);
     float *ws_lse = reinterpret_cast<float *>(ws_o + align256(sh.splits * rows * D * 2));
-    if ((rc = launch(sh, q, k, v, ws_o, ws_lse, Hkv, Skv, D, scale, dtype, 0, status, st)) != SDP_OK)
+    if ((rc = launch(sh, q, k, v, ws_o, ws_lse, Hkv, Skv, D, scale, dtype, 0, status, sms, st)) != SDP_OK)
         return rc;
     return sdp_merge(ws_o, ws_lse, sh.splits, rows, D, dtype, o, lse, stream);
 }
@@ -552,12 +599,11 @@ int sdp_poll_status(void *stream)
         return cuda_fail(e);
     if (word == 0)
         return SDP_OK;
-    g_last_detail.store(word);
     if ((e = cudaMemset(status, 0, sizeof(unsigned int))) != cudaSuccess)
         return cuda_fail(e);
     if ((e = cudaDeviceSynchronize()) != cudaSuccess)
         return cuda_fail(e);
-    return (word & 0xffu) == 7u ? SDP_ERR_BAD_SEQLENS : SDP_ERR_DEVICE_TIMEOUT;
+    return sdp::status_code_of(word);
 }
 
 unsigned int sdp_last_status_detail(void) { return g_last_detail.load(); }
@@ -594,7 +640,7 @@ const char *sdp_strerror(int code)
     }
 }
 
-int sdp_version(void) { return 104; }
+int sdp_version(void) { return 105; }
 
 void sdp_shutdown(void)
 {
@@ -603,6 +649,7 @@ void sdp_shutdown(void)
         for (MapEntry &e : g_map_cache)
             e.valid = false;
     }
+    sdp::noalloc_forget();
     std::lock_guard<std::mutex> lk(g_mu);
     int cur = 0;
     const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;

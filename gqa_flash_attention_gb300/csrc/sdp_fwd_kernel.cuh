@@ -836,8 +836,10 @@ template <int D, bool BF16>
 cudaError_t launch_sdp_fwd(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o,
                            const KernelParams &p, int grid, cudaStream_t stream)
 {
-    auto kern = p.cu_q != nullptr ? sdp_fwd_kernel<D, BF16, true> : sdp_fwd_kernel<D, BF16, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::SMEM_BYTES);
+    static unsigned long long set_dense = 0, set_varlen = 0;
+    const bool vl = p.cu_q != nullptr;
+    auto kern = vl ? sdp_fwd_kernel<D, BF16, true> : sdp_fwd_kernel<D, BF16, false>;
+    cudaError_t e = set_smem_once(kern, Layout<D>::SMEM_BYTES, vl ? set_varlen : set_dense);
     if (e != cudaSuccess)
         return e;
     kern<<<grid, NUM_THREADS, Layout<D>::SMEM_BYTES, stream>>>(q, k, v, o, p);

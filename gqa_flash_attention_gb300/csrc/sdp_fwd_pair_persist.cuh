@@ -502,20 +502,12 @@ template <int D, bool BF16>
 cudaError_t launch_sdp_fwd_pair_persistent(const CUtensorMap &q, const CUtensorMap &k_half, const CUtensorMap &v,
                                            const KernelParams &p, int grid, cudaStream_t stream)
 {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess)
-            return e;
-    }
+    static unsigned long long set = 0;
     auto kern = sdp_fwd_pair_persistent_kernel<D, BF16>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairLayout<D>::SMEM_BYTES);
+    cudaError_t e = set_smem_once(kern, PairLayout<D>::SMEM_BYTES, set);
     if (e != cudaSuccess)
         return e;
+    const int sms = p.num_sms;
     const int clusters = grid / 2 < sms / 2 ? grid / 2 : sms / 2;
     kern<<<2 * clusters, NUM_THREADS, PairLayout<D>::SMEM_BYTES, stream>>>(q, k_half, v, p);
     return cudaGetLastError();
@@ -527,10 +519,7 @@ inline bool use_persistent(const KernelParams &p, int grid)
 {
     if (p.debug_flags & DEBUG_NO_PERSIST)
         return false;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return false;
-    return !p.causal && p.cu_q == nullptr && p.kv_splits == 1 && p.o != nullptr && grid > sms;
+    return !p.causal && p.cu_q == nullptr && p.kv_splits == 1 && p.o != nullptr && p.num_sms > 0 && grid > p.num_sms;
 }
 
 }  // namespace sdp

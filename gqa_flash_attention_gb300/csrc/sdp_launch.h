@@ -35,6 +35,9 @@ struct KernelParams {
     // (sum over the nseq sequences of ceil(rows / 128)); slots past the last
     // real tile return at once. 0: the grid covers n_qtiles tiles per sequence.
     int nseq, n_tiles;
+    // Host-side facts of the launching device (not read by the kernels): its
+    // SM count, cached per device so that a launch makes no attribute query.
+    int num_sms;
 };
 
 // Sequences per batch up to which causal variable-length launches use the compact
@@ -57,5 +60,43 @@ SDP_DECLARE_LAUNCH(launch_d256_fp16)
 SDP_DECLARE_LAUNCH(launch_d256_bf16)
 
 #undef SDP_DECLARE_LAUNCH
+
+// Where a launch's status word comes from: called for the current device `dev`
+// once every argument check has passed, it returns the word's device address
+// (zeroed, or zeroed in stream order before the kernel) or a status code.
+using StatusSource = int (*)(int dev, unsigned int **status, cudaStream_t stream);
+
+// The dense forward of sdp_fwd / sdp_fwd_causal: validation, the launch shape
+// (head packing), tensor maps and the kernel launch, with the status word from
+// `status_of`. Nothing is launched and `status_of` is not called when a check
+// fails.
+int forward_with(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
+                 int Skv, int D, float scale, int dtype, int causal, StatusSource status_of, void *stream);
+
+// Records `word` as the status detail that sdp_last_status_detail() returns and
+// maps it to its status code (SDP_ERR_BAD_SEQLENS or SDP_ERR_DEVICE_TIMEOUT).
+int status_code_of(unsigned int word);
+
+// Forgets the per-device addresses that sdp_fwd_noalloc looked up (called by
+// sdp_shutdown, after which a reset device may hold the array elsewhere).
+void noalloc_forget();
+
+// Sets the cudaFuncAttributeMaxDynamicSharedMemorySize of a kernel once per
+// device (`done` is that kernel's bit mask of devices already set).
+template <typename Kernel>
+cudaError_t set_smem_once(Kernel kern, int bytes, unsigned long long &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit != 0 && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit != 0)
+        __atomic_fetch_or(&done, bit, __ATOMIC_RELEASE);
+    return e;
+}
 
 }  // namespace sdp

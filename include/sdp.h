@@ -193,8 +193,10 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
  * synchronisation is not acceptable. This call allocates nothing: no
  * cudaMalloc, no cudaFree, no allocating library routine.
  *
- * Arguments, layout, ownership, validation and results are exactly those of
- * sdp_fwd, and it launches the same kernel. The kernel's only scratch, its
+ * Arguments, layout, ownership, validation and results are those of sdp_fwd,
+ * and the launch is sdp_fwd's own: the same head packing, the same kernel
+ * choice, the same wait limit (sdp_set_wait_timeout_ms) and debug flags, so the
+ * outputs are bit for bit those of sdp_fwd. The kernel's only scratch, its
  * status word, lives in a static device array of SDP_NOALLOC_SCRATCH_BYTES
  * inside the library, which every GPU that loads the library holds until the
  * process exits. A launch needs 4 bytes of it whatever the problem size; a
@@ -202,19 +204,29 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
  *
  * Set-up: the first call on each device (made with that device current)
  * looks up the device address of the array with cudaGetSymbolAddress and
- * caches it; make that first call before any stream capture.
+ * caches it (sdp_shutdown forgets it); make that first call before any stream
+ * capture.
  *
  * Sharing: every call in the process uses the same array. Each call clears
- * the status word on `stream` before its kernel, so calls that overlap on the
- * GPU (different streams without ordering between them) race on it. A wait
- * timeout inside this call (2 s per wait) leaves the affected output tile
- * unwritten and is recorded only in that shared word: sdp_poll_status does
- * not report it.
+ * the status word on `stream` before its kernel (a 4-byte cudaMemsetAsync), so
+ * calls that overlap on the GPU (different streams without ordering between
+ * them) race on it. A wait that times out inside the kernel leaves its output
+ * tile unwritten and records the event in that word, not in the word that
+ * sdp_poll_status reads: read it with sdp_fwd_noalloc_status.
  */
 #define SDP_NOALLOC_SCRATCH_BYTES 256
 int sdp_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
                     int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale, int dtype,
                     void *stream);
+
+/*
+ * sdp_fwd_noalloc_status — synchronise `stream`, then read and clear the status
+ * word of sdp_fwd_noalloc's shared array on the current device (as the last
+ * such call that finished left it). Allocates nothing (cudaMemcpyFromSymbol /
+ * cudaMemcpyToSymbol of 4 bytes). Returns SDP_OK, SDP_ERR_DEVICE_TIMEOUT (a
+ * wait gave up; the detail is then in sdp_last_status_detail) or SDP_ERR_CUDA.
+ */
+int sdp_fwd_noalloc_status(void *stream);
 
 /*
  * sdp_poll_status — synchronise `stream`, then read and clear the current
@@ -262,7 +274,8 @@ int sdp_last_cuda_error(void);
 /* A static, human-readable description of a status code. */
 const char *sdp_strerror(int code);
 
-/* ABI version: 100 * major + minor (101: sdp_fwd_causal; 102: sdp_merge; 103: split-KV; 104: varlen). */
+/* ABI version: 100 * major + minor (101: sdp_fwd_causal; 102: sdp_merge; 103: split-KV; 104: varlen;
+ * 105: sdp_fwd_noalloc_status). */
 int sdp_version(void);
 
 /* Free the per-device status words and forget the cached tensor maps (host

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_version_and_messages(L):
-    assert L.sdp_version() == 104
+    assert L.sdp_version() == 105
     for code in range(-7, 1):
         assert len(sdp.strerror(code)) > 0
     assert sdp.strerror(-99) == "unknown status code"
@@ -59,7 +59,7 @@ def call(**kw):
     return sdp.sdp_fwd_ptr(**args)
 
 
-@pytest.mark.parametrize("kw,code", [
+DENSE_BAD = [
     (dict(D=64), sdp.SDP_ERR_UNSUPPORTED),
     (dict(D=192), sdp.SDP_ERR_UNSUPPORTED),
     (dict(dtype=2), sdp.SDP_ERR_UNSUPPORTED),
@@ -80,9 +80,21 @@ def call(**kw):
     (dict(lse=5 * A + 2), sdp.SDP_ERR_ALIGNMENT),
     (dict(B=1 << 16, Hq=1 << 16, Hkv=1), sdp.SDP_ERR_OVERFLOW),
     (dict(B=1 << 10, Hq=1 << 12, Hkv=1, Sq=1 << 20), sdp.SDP_ERR_OVERFLOW),
-])
+]
+
+
+@pytest.mark.parametrize("kw,code", DENSE_BAD)
 def test_validation_errors_launch_nothing(L, kw, code):
     assert call(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", DENSE_BAD)
+def test_noalloc_validates_like_sdp_fwd(L, kw, code):
+    # the allocation-free entry point runs sdp_fwd's own checks, before any CUDA call
+    args = dict(q=A, k=2 * A, v=3 * A, o=4 * A, lse=5 * A, B=1, Hq=4, Hkv=1, Sq=256, Skv=256, D=128,
+                scale=0.088, dtype=sdp.SDP_FP16)
+    args.update(kw)
+    assert sdp.sdp_fwd_noalloc_ptr(**args) == code
 
 
 def test_python_binding_rejects_bad_tensors():

@@ -1,6 +1,9 @@
 """sdp_fwd_noalloc: the entry point for callers that cannot allocate device
 memory (their memory belongs to their own pool or host application), checked
 through the C ABI against sdp_fwd on the same inputs, on two calls in a row.
+It takes sdp_fwd's own launch, so its outputs are bit for bit sdp_fwd's,
+including where that launch packs heads (decode) or runs the persistent
+kernel; its timeouts are read back with sdp_fwd_noalloc_status.
 
 This file is collected last on purpose, so that a run stopping at the first
 failure has run every other test first. It also passes on its own in a fresh
@@ -34,10 +37,11 @@ def _inputs(w):
     return q, k, v
 
 
-def _noalloc(q, k, v, w):
+def _noalloc(q, k, v, w, with_lse=True):
     o = torch.full_like(q, float("nan"))
-    lse = torch.full((w.B, w.Hq, w.Sq), float("nan"), dtype=torch.float32, device=q.device)
-    rc = sdp.sdp_fwd_noalloc_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+    lse = torch.full((w.B, w.Hq, w.Sq), float("nan"), dtype=torch.float32, device=q.device) if with_lse else None
+    rc = sdp.sdp_fwd_noalloc_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr() if with_lse else 0,
                                  w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.softmax_scale, CODE[w.dtype],
                                  torch.cuda.current_stream().cuda_stream)
     assert rc == sdp.SDP_OK, sdp.strerror(rc)
@@ -72,6 +76,53 @@ def test_two_calls_in_a_row_match_sdp_fwd():
     for o, lse in ((o1, l1), (o2, l2)):
         st = compare(o, lse, refs[0][0].double().cpu().numpy(), refs[0][1].double().cpu().numpy(), w.dtype)
         assert_within(st, w.dtype)
+    # same launch as sdp_fwd: bit for bit
+    for (o, lse), (o_ref, l_ref) in zip(outs, refs):
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+    assert sdp.noalloc_status() == sdp.SDP_OK
+
+
+@pytest.mark.parametrize("w", [
+    # 160 units of a dense D=256 launch: sdp_fwd runs the persistent CTA-pair kernel here
+    Workload("noalloc_persistent", 1, 8, 2, 2560, 384, 256, "fp16", seed=53),
+    # decode: one query row, 16 heads per KV head, packed into one 16-row tile
+    Workload("noalloc_decode", 1, 16, 1, 1, 1000, 256, "fp16", seed=54),
+    Workload("noalloc_decode_bf16", 2, 8, 2, 3, 777, 128, "bf16", seed=55),
+], ids=lambda w: w.name)
+def test_same_launch_as_sdp_fwd_bit_for_bit(w):
+    q, k, v = _inputs(w)
+    o_ref, l_ref = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale)
+    o, lse = _noalloc(q, k, v, w)
+    o_nl, _ = _noalloc(q, k, v, w, with_lse=False)  # LSE is optional, as for sdp_fwd
+    torch.cuda.synchronize()
+    assert sdp.noalloc_status() == sdp.SDP_OK
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+    assert torch.equal(o_nl, o_ref)
+
+
+def test_timeout_is_read_back_and_the_next_call_is_right():
+    # Debug flag 1: the load warp issues no copies, so every wait runs out after the 50 ms
+    # limit (a bounded wait on a barrier nothing completes; no fault). The timeout lands in
+    # this entry point's own status word, which sdp_fwd_noalloc_status reads and clears.
+    w = CASES[0]
+    q, k, v = _inputs(w)
+    assert sdp.noalloc_status() == sdp.SDP_OK
+    assert sdp.poll_status() == sdp.SDP_OK
+    old_ms = sdp.set_wait_timeout_ms(50)
+    old_flags = sdp.set_debug_flags(1)
+    try:
+        _noalloc(q, k, v, w)
+        assert sdp.noalloc_status() == sdp.SDP_ERR_DEVICE_TIMEOUT
+        assert 1 <= (sdp.last_status_detail() & 0xFF) <= 6, hex(sdp.last_status_detail())
+    finally:
+        sdp.set_debug_flags(old_flags)
+        sdp.set_wait_timeout_ms(old_ms)
+    assert sdp.noalloc_status() == sdp.SDP_OK  # cleared
+    assert sdp.poll_status() == sdp.SDP_OK     # sdp_fwd's word was not touched
+    o_ref, l_ref = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale)
+    o, lse = _noalloc(q, k, v, w)
+    assert sdp.noalloc_status() == sdp.SDP_OK
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
 
 
 def test_rejects_bad_arguments_without_launching():
