@@ -401,8 +401,17 @@ def kernel_name(w):
     units than SMs, else the single-CTA kernel; split-KV adds the merge kernel;
     variable-length batches pair up when the group size is even; head dim 128
     always runs on single CTAs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
     if w.D == 128:
-        name = "sdp_fwd_kernel"  # the single-CTA kernel is as fast or faster at D=128
+        # dense, non-causal launches whose two-tile units pair up and fill a wave of CTAs run the
+        # two-tile CTA-pair kernel; the rest the single-CTA kernel
+        name = "sdp_fwd_kernel"
+        if PAIR2_BY_DEFAULT and not is_varlen(w) and not w.causal:
+            sq, G = launch_shape(w)
+            n_qpairs = ((sq + 127) // 128 + 1) // 2
+            splits = max(1, w.kv_splits)
+            if (n_qpairs * G) % 2 == 0 and w.B * w.Hkv * G * n_qpairs * splits >= sms:
+                name = "sdp_fwd_pair2_kernel"
         return name + " + merge_kernel" if getattr(w, "kv_splits", 1) != 1 else name
     if is_varlen(w):
         return "sdp_fwd_pair_kernel" if (w.Hq // w.Hkv) % 2 == 0 else "sdp_fwd_kernel"
@@ -414,11 +423,13 @@ def kernel_name(w):
         return name + " + merge_kernel"
     # dense, non-causal CTA-pair launches with more units than SMs run the persistent form
     units = w.B * w.Hkv * G * n_qtiles
-    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
     if pair and not w.causal and units > sms:
         return "sdp_fwd_pair_persistent_kernel"
     return name
 
+
+# whether the library runs dense D=128 launches on the two-tile CTA-pair kernel by default
+PAIR2_BY_DEFAULT = False
 
 L2_BYTES = 126 * 2 ** 20
 

@@ -10,6 +10,7 @@ library is missing or the device is not sm_103, calls raise.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -98,6 +99,14 @@ def _check(rc: int) -> None:
         raise SdpError(rc, msg)
 
 
+def _on(device):
+    """The device context of a call: none when `device` is already current (entering
+    torch.cuda.device costs microseconds per call)."""
+    if device.index is None or device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 def _stream_handle(stream, device) -> int:
     if stream is None:
         return torch.cuda.current_stream(device).cuda_stream
@@ -183,7 +192,7 @@ def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
     if kv_splits != 1:
         if causal:
             raise ValueError("the split-KV forward has no causal mask")
-        with torch.cuda.device(q.device):
+        with _on(q.device):
             dt = _DTYPE_CODE[q.dtype]
             need = splitkv_workspace_bytes(B, Hq, Hkv, Sq, Skv, D, dt, kv_splits)
             if workspace is None:
@@ -199,7 +208,7 @@ def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
                                      _stream_handle(stream, q.device))
         _check(rc)
         return out, lse
-    with torch.cuda.device(q.device):
+    with _on(q.device):
         rc = sdp_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                          0 if lse is None else lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
                          _DTYPE_CODE[q.dtype], _stream_handle(stream, q.device), causal=causal)
@@ -258,7 +267,7 @@ def sdp_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
     if lse is not None and (lse.shape != (Hq, total_q) or lse.dtype != torch.float32 or not lse.is_contiguous()
                             or lse.device != q.device):
         raise ValueError("lse must be a contiguous float32 tensor [Hq, total_q] on q's device")
-    with torch.cuda.device(q.device):
+    with _on(q.device):
         rc = sdp_fwd_varlen_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                 0 if lse is None else lse.data_ptr(), cu_seqlens_q.data_ptr(),
                                 cu_seqlens_k.data_ptr(), cu_seqlens_q.numel() - 1, Hq, Hkv, total_q, total_k,
@@ -290,7 +299,7 @@ def sdp_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor 
         out = torch.empty(o_parts.shape[1:], dtype=o_parts.dtype, device=o_parts.device)
     if lse is None and return_lse:
         lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
-    with torch.cuda.device(o_parts.device):
+    with _on(o_parts.device):
         rc = int(lib().sdp_merge(ctypes.c_void_p(o_parts.data_ptr()), ctypes.c_void_p(lse_parts.data_ptr()), int(P),
                                  int(rows), int(D), _DTYPE_CODE[o_parts.dtype], ctypes.c_void_p(out.data_ptr()),
                                  ctypes.c_void_p(0 if lse is None else lse.data_ptr()),
@@ -321,8 +330,11 @@ def set_debug_flags(flags: int) -> int:
     2: never the CTA-pair kernel; 4: never pack a group's query heads; 8: the
     CTA-pair kernel at head dim 128 too; 16: one CTA pair per unit where the
     persistent kernel would run; 32: variable-length launches on the full grid
-    instead of the compact tile list. 4, 16 and 32 give bit-identical results;
-    2 and 8 switch kernels that compute the same function.
+    instead of the compact tile list; 64: never the two-tile CTA-pair kernel at
+    head dim 128; 128: the two-tile CTA-pair kernel (two query tiles per CTA,
+    64-key steps) for dense non-causal head-dim-128 launches whose units pair.
+    4, 16 and 32 give bit-identical results; 2, 8 and 128 switch kernels that
+    compute the same function.
     """
     return int(lib().sdp_set_debug_flags(int(flags)))
 

@@ -484,6 +484,23 @@ __device__ __forceinline__ float lg2(float x)
     return y;
 }
 
+// Per-thread register limit of the executing warpgroup (all four of its warps
+// execute it): raise it by taking registers from the block's pool, or lower it
+// to return registers to the pool. The sum over warpgroups must stay within the
+// block's allocation at launch (threads x registers per thread).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -326,6 +326,8 @@ int launch(const Shape &sh, const void *q, const void *k, const void *v, void *o
         (rc = encode_map(&maps.v, v, dtype, D, Skv, sh.planes_kv)) != SDP_OK ||
         (rc = encode_map(&maps.o, o, dtype, D, sh.Sq, out_planes)) != SDP_OK)
         return rc;
+    if (D == 128 && (rc = encode_map(&maps.k32, k, dtype, D, Skv, sh.planes_kv, 32)) != SDP_OK)
+        return rc;
 
     sdp::KernelParams p{};
     p.lse = lse;

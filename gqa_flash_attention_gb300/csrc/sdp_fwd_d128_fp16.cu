@@ -1,11 +1,13 @@
 // Instantiation of the attention forward kernels: head dim 128, fp16 I/O.
-#include "sdp_fwd_pair.cuh"
+#include "sdp_fwd_pair2.cuh"
 #include "sdp_launch.h"
 
 namespace sdp {
 
 cudaError_t launch_d128_fp16(const LaunchMaps &m, const KernelParams &p, int grid, cudaStream_t stream)
 {
+    if (!(p.debug_flags & DEBUG_PAIR_D128) && use_pair2(p, grid))
+        return launch_sdp_fwd_pair2<false>(m.q, m.k32, m.v, m.o, p, stream);
     if (use_pair(p, grid, 128))
         return launch_sdp_fwd_pair<128, false>(m.q, m.k_half, m.v, m.o, p, grid, stream);
     return launch_sdp_fwd<128, false>(m.q, m.k, m.v, m.o, p, grid, stream);

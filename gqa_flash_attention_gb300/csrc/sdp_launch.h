@@ -44,10 +44,11 @@ struct KernelParams {
 // unit list (its level-order search holds two sequences per lane in registers).
 constexpr int VARLEN_LEVEL_MAX_SEQS = 64;
 
-// Tensor maps of one launch: Q, K, V, O with 128-row boxes, and K with 64-row
-// boxes (half a KV tile) for the CTA-pair kernel.
+// Tensor maps of one launch: Q, K, V, O with 128-row boxes, K with 64-row
+// boxes (half a KV tile) for the CTA-pair kernel, and (dense launches at head
+// dim 128) K with 32-row boxes for the two-tile CTA-pair kernel.
 struct LaunchMaps {
-    CUtensorMap q, k, k_half, v, o;
+    CUtensorMap q, k, k_half, k32, v, o;
 };
 
 // Launches the CTA-pair kernel when consecutive units pair up within one

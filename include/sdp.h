@@ -264,7 +264,11 @@ unsigned int sdp_set_wait_timeout_ms(unsigned int ms);
  * per unit even where the persistent CTA-pair kernel applies (same result, bit
  * for bit). Bit 5: variable-length launches cover the longest sequence's query
  * tiles for every sequence instead of the list of tiles that exist (same
- * result, bit for bit). Returns the previous flags.
+ * result, bit for bit). Bit 6: at head dim 128, never the two-tile CTA-pair
+ * kernel. Bit 7: at head dim 128, run dense non-causal launches whose two-tile
+ * units pair up on the two-tile CTA-pair kernel (two 128-row query tiles per
+ * CTA, 64-key softmax steps; the same function, rounded differently), even
+ * below one wave of CTAs. Returns the previous flags.
  */
 int sdp_set_debug_flags(int flags);
 

@@ -33,7 +33,9 @@ def _built():
     (DEBUG_NO_LOADS | DEBUG_SINGLE_CTA, Workload("timeout", 1, 4, 2, 256, 384, 128, "fp16", seed=91)),
     # 160 units of a dense D=256 launch: the persistent CTA-pair kernel
     (DEBUG_NO_LOADS, Workload("timeout_persist", 1, 8, 2, 2560, 384, 256, "fp16", seed=92)),
-], ids=["cta_pair", "single_cta", "persistent_pair"])
+    # the two-tile CTA-pair kernel at D=128 (debug flag 128 forces it below one wave)
+    (DEBUG_NO_LOADS | 128, Workload("timeout_pair2", 1, 4, 2, 256, 384, 128, "bf16", seed=93)),
+], ids=["cta_pair", "single_cta", "persistent_pair", "two_tile_pair"])
 def test_wait_timeout_is_reported_and_the_context_survives(flags, w):
     q, k, v = (t.cuda() for t in workloads.make_inputs(w))
     assert sdp.poll_status() == sdp.SDP_OK
