@@ -76,7 +76,7 @@ struct Pair2Layout {
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
     static_assert(8 * NBARS + 8 <= BAR_AREA, "barrier area");
     // Each issuer waits for every K and V chunk in the order 0, 2, 1, 3, 4, 5, ...
-    // (K_0, V_0, K_1, K_2?, ...): when it waits for position P it has already seen
+    // (K_0, V_0, K_1, K_2, V_1, ...): when it waits for position P it has already seen
     // every position up to P - 2 land, so the chunk NSLOTS before P has landed and
     // the slot's parity cannot alias.
     static_assert(NSLOTS >= 3, "ring parity soundness");
@@ -253,14 +253,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair2Layout::THREADS
             const uint64_t dk = ptx::smem_desc_sw128(s_ring, 16, 1024);
             const uint64_t dv = ptx::smem_desc_sw128(s_ring, L::HALF_BYTES, 1024);
             bool issued = false;
-            // S_x(t): buffer t mod 2; K tile t / 2, this half's 32 keys in each CTA.
-            auto issue_s = [&](int t) -> bool {
+            // Ring slots are waited for ahead of use, while the issuer would otherwise wait for
+            // the next P: a barrier round trip costs ~200 cycles under tensor load even when the
+            // chunk has landed, and here it stays off the P -> PV -> S chain. Slots are waited in
+            // the order K_0, V_0, K_1, K_2, V_1, K_3, V_2, ...: positions 0, 2, 1, 3, 4, 5, 6, ...
+            auto wait_slot = [&](int pos) -> bool {
+                return __all_sync(0xffffffffu,
+                                  wait_bounded(slot_full0 + 8u * (pos % NS), (pos / NS) & 1, cx, SITE_SLOT_FULL));
+            };
+            // S_x(t): buffer t mod 2; K tile t / 2 (its slot waited for), this half's 32 keys in each CTA.
+            auto issue_s = [&](int t) {
                 const int j = t >> 1, h = t & 1;
-                const int pos = pos_k<1>(j);
-                const int slot = pos % NS;
-                if (h == 0 &&
-                    !__all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL)))
-                    return false;
+                const int slot = pos_k<1>(j) % NS;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + pair2_s_col(x, t & 1);
                 const uint64_t kslot = dk + static_cast<uint64_t>((slot * L::HALF_BYTES + h * L::K_HALF_OFF) >> 4);
@@ -274,16 +278,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair2Layout::THREADS
                 ptx::mma_commit_pair_w(s_full0 + 8u * (2 * x + (t & 1)));
                 if (h == 1 || t == n - 1)
                     ptx::mma_commit_pair_w(slot_empty0 + 8u * slot);  // this tile's last read of K_j
-                return true;
             };
-            // O_x += P_x(s) V: V tile s / 2, keys 64 (s mod 2) + [0, 64) as four K steps of 16.
+            // O_x += P_x(s) V: V tile s / 2 (its slot waited for), keys 64 (s mod 2) + [0, 64) in K steps of 16.
             auto issue_pv = [&](int s) -> bool {
                 const int j = s >> 1, h = s & 1;
-                const int pos = pos_v<1>(j, n_tiles);
-                const int slot = pos % NS;
-                if (h == 0 &&
-                    !__all_sync(0xffffffffu, wait_bounded(slot_full0 + 8u * slot, (pos / NS) & 1, cx, SITE_SLOT_FULL)))
-                    return false;
+                const int slot = pos_v<1>(j, n_tiles) % NS;
                 const uint32_t pbar = s + 1 < n ? p_full0 + 8u * (2 * x + (s & 1)) : p_last0 + 8u * x;
                 const uint32_t ppar = s + 1 < n ? static_cast<uint32_t>((s >> 1) & 1) : 0u;
                 if (!__all_sync(0xffffffffu, wait_bounded(pbar, ppar, cx, SITE_P_FULL)))
@@ -301,25 +300,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair2Layout::THREADS
                     ptx::mma_commit_pair_w(slot_empty0 + 8u * slot);  // this tile's last read of V_j
                 return true;
             };
-            bool ok = __all_sync(0xffffffffu, wait_bounded(q_full0 + 8u * x, 0, cx, SITE_Q_FULL));
-            if (ok)
-                ok = issue_s(0);
-            if (ok && n > 1)
-                ok = issue_s(1);
+            bool ok = __all_sync(0xffffffffu, wait_bounded(q_full0 + 8u * x, 0, cx, SITE_Q_FULL)) && wait_slot(0);
+            if (ok) {
+                issue_s(0);
+                if (n > 1)
+                    issue_s(1);
+                ok = wait_slot(pos_v<1>(0, n_tiles)) && (n <= 2 || wait_slot(pos_k<1>(1)));  // V_0; K_1 for S(2), S(3)
+            }
             for (int s = 0; ok && s < n; ++s) {
                 if (!(ok = issue_pv(s)))
                     break;
                 // S(2) overwrites S(0)'s buffer, whose scores the softmax read before P(0).
-                if (s == 0 && n > 2 && !(ok = issue_s(2)))
-                    break;
+                if (s == 0 && n > 2)
+                    issue_s(2);
                 // S(s+3) overwrites buffer (s+1) mod 2: S(s+1) (read before P(s) was stored)
                 // and P(s) in its upper half, which PV(s) must have consumed.
                 if (s + 3 < n) {
                     if (!(ok = __all_sync(0xffffffffu, wait_bounded(o_done0 + 8u * (RING * x + s % RING),
                                                                     (s / RING) & 1, cx, SITE_O_DONE))))
                         break;
-                    ok = issue_s(s + 3);
+                    issue_s(s + 3);
                 }
+                // the slots of the next PV and the S after it, while P(s+1) is being computed
+                if (s + 1 < n && ((s + 1) & 1) == 0 && !(ok = wait_slot(pos_v<1>((s + 1) >> 1, n_tiles))))
+                    break;
+                if (s + 4 < n && ((s + 4) & 1) == 0 && !(ok = wait_slot(pos_k<1>((s + 4) >> 1))))
+                    break;
             }
             if (issued) {  // all of this thread's MMAs complete before TMEM is freed
                 ptx::mma_commit_pair_w(final0 + 8u * x);
