@@ -56,7 +56,6 @@ constexpr int DEBUG_NO_LOADS = 1;
 constexpr int DEBUG_SINGLE_CTA = 2;  // never use the CTA-pair kernel
 constexpr int DEBUG_PAIR_D128 = 8;   // use the CTA-pair kernel at D=128 too, where it qualifies
 constexpr int DEBUG_NO_PERSIST = 16; // one unit per CTA pair even where the persistent form applies
-constexpr int DEBUG_NO_LOOKAHEAD = 256;  // single-CTA softmax: no next-tile row extreme during the exponentials
 constexpr int NUM_THREADS = 256;
 constexpr int O_DONE_RING = 4;  // PV completion barriers, used round robin
 
@@ -95,39 +94,6 @@ struct Layout {
     // those sits 1 to 3 positions before the waited chunk, never NSLOTS >= 4.
     static_assert(NSLOTS >= 4 && (CHUNKS_PER_TILE == 1 ? NSBUF <= 3 : NSBUF == 2), "ring parity soundness");
 };
-
-// Row extreme of N raw scores, four three-input chains: the maximum, or (a negative
-// scale, MAX false) the minimum, whose product with the scale is the maximum of the
-// scaled scores. Exact whatever the grouping, so any split of a row gives the same value.
-template <bool MAX, int N>
-__device__ __forceinline__ float row_extreme(const float *v)
-{
-    static_assert(N % 8 == 0 && N >= 16, "row length");
-    float m0 = v[0], m1 = v[1], m2 = v[2], m3 = v[3];
-#pragma unroll
-    for (int i = 4; i < N - 4; i += 8) {
-        if constexpr (MAX) {
-            m0 = ptx::max3(m0, v[i], v[i + 1]);
-            m1 = ptx::max3(m1, v[i + 2], v[i + 3]);
-            m2 = ptx::max3(m2, v[i + 4], v[i + 5]);
-            m3 = ptx::max3(m3, v[i + 6], v[i + 7]);
-        } else {
-            m0 = ptx::min3(m0, v[i], v[i + 1]);
-            m1 = ptx::min3(m1, v[i + 2], v[i + 3]);
-            m2 = ptx::min3(m2, v[i + 4], v[i + 5]);
-            m3 = ptx::min3(m3, v[i + 6], v[i + 7]);
-        }
-    }
-    if constexpr (MAX) {
-        m0 = ptx::max3(m0, v[N - 4], v[N - 3]);
-        m1 = ptx::max3(m1, v[N - 2], v[N - 1]);
-        return ptx::max3(m0, m1, fmaxf(m2, m3));
-    } else {
-        m0 = ptx::min3(m0, v[N - 4], v[N - 3]);
-        m1 = ptx::min3(m1, v[N - 2], v[N - 1]);
-        return ptx::min3(m0, m1, fminf(m2, m3));
-    }
-}
 
 // Lazy rescale threshold in base-2 units: the running maximum is only moved
 // when a tile's maximum exceeds it by more than this, so P <= 2^8.
@@ -665,11 +631,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         bool s_seen = false;  // S_j's barrier was seen complete while tile j-1 ended
-        // Row extreme of tile j's raw scores, already found during tile j-1's exponentials
-        // (when tile j holds no masked key): the next tile's scores are loaded and reduced
-        // between the exponential quarters, so the maximum is off the tile's critical path.
-        bool have_mx = false;
-        float mx_next = 0.f;
 
         for (int j = 0; j < n; ++j) {
             const int buf = j % NB;
@@ -703,8 +664,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (i >= valid)
                         s[i] = s[0];  // neutral for the max; weights zeroed below
             }
-            // Row extreme of the raw scores (maximum of s * c: of s when c >= 0, else its minimum).
-            const float mx0 = have_mx ? mx_next : (c >= 0.f ? row_extreme<true, 128>(s) : row_extreme<false, 128>(s));
+            // Row extreme of the raw scores (maximum of s * c: of s when c >= 0, else
+            // its minimum), four three-input chains.
+            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+            if (c >= 0.f) {
+#pragma unroll
+                for (int i = 4; i < 124; i += 8) {
+                    mx0 = ptx::max3(mx0, s[i], s[i + 1]);
+                    mx1 = ptx::max3(mx1, s[i + 2], s[i + 3]);
+                    mx2 = ptx::max3(mx2, s[i + 4], s[i + 5]);
+                    mx3 = ptx::max3(mx3, s[i + 6], s[i + 7]);
+                }
+                mx0 = ptx::max3(mx0, s[124], s[125]);
+                mx1 = ptx::max3(mx1, s[126], s[127]);
+                mx0 = ptx::max3(mx0, mx1, fmaxf(mx2, mx3));
+            } else {
+#pragma unroll
+                for (int i = 4; i < 124; i += 8) {
+                    mx0 = ptx::min3(mx0, s[i], s[i + 1]);
+                    mx1 = ptx::min3(mx1, s[i + 2], s[i + 3]);
+                    mx2 = ptx::min3(mx2, s[i + 4], s[i + 5]);
+                    mx3 = ptx::min3(mx3, s[i + 6], s[i + 7]);
+                }
+                mx0 = ptx::min3(mx0, s[124], s[125]);
+                mx1 = ptx::min3(mx1, s[126], s[127]);
+                mx0 = ptx::min3(mx0, mx1, fminf(mx2, mx3));
+            }
             const float m_tile = mx0 * c;  // this tile's row maximum of s * scale * log2(e)
             const float m_new = (j == 0 || m_tile > m_used + RESCALE_THRESHOLD) ? m_tile : m_used;
             const float alpha = (j == 0 || m_new == m_used) ? 1.f : ptx::ex2(m_used - m_new);
@@ -715,11 +700,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t pk[64];
             const uint64_t c2 = ptx::f2_pack(c, c), negm2 = ptx::f2_pack(neg_m, neg_m);
             uint64_t sum01 = ptx::f2_pack(0.f, 0.f), sum23 = sum01;
-            // pk words [lo, hi), i.e. scores [2 lo, 2 hi), in order (the running sums are
-            // the same sequence of additions however the range is cut)
-            auto exp_range = [&](auto masked, auto lo, auto hi) {
+            auto exp_tile = [&](auto masked) {
 #pragma unroll
-                for (int i = decltype(lo)::value; i < decltype(hi)::value; i += 2) {
+                for (int i = 0; i < 64; i += 2) {
                     float x0, x1, x2, x3;
                     ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i], s[2 * i + 1]), c2, negm2), x0, x1);
                     ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * i + 2], s[2 * i + 3]), c2, negm2), x2, x3);
@@ -739,73 +722,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     pk[i + 1] = pack2<BF16>(p2, p3);
                 }
             };
-            using I0 = std::integral_constant<int, 0>;
-            using I16 = std::integral_constant<int, 16>;
-            using I32 = std::integral_constant<int, 32>;
-            using I48 = std::integral_constant<int, 48>;
-            using I64 = std::integral_constant<int, 64>;
-            // Lookahead when tile j+1 exists and holds no masked key (so its extreme needs no
-            // per-key test); a masked tile j is the last one, so it never looks ahead. Only
-            // with three score buffers (D=128): with two, S_{j+1} waits for PV_{j-1} and is
-            // not ready during tile j.
-            const bool look = NB >= 3 && j + 1 < n && !tail && !(p.debug_flags & DEBUG_NO_LOOKAHEAD) &&
-                              !__any_sync(0xffffffffu, valid - L::BN < L::BN);
-            have_mx = false;
-            if constexpr (NB < 3) {
-                if (tail)
-                    exp_range(std::true_type{}, I0{}, I64{});
-                else
-                    exp_range(std::false_type{}, I0{}, I64{});
-                s_seen = j + 1 < n && ptx::mbar_test_wait(s_full0 + 8u * ((j + 1) % NB), ((j + 1) / NB) & 1);
-            } else if (look) {
-                // S_{j+1} completed long ago in the steady state (it waited only for PV_{j+1-NSBUF}).
-                ok = __all_sync(0xffffffffu, wait_bounded(s_full0 + 8u * ((j + 1) % NB), ((j + 1) / NB) & 1, cx,
-                                                          SITE_S_FULL));
-                if (!ok)
-                    break;
-                ptx::tc_fence_after();
-                const uint32_t ts1 = t_s + ((j + 1) % NB) * L::BN;
-                // tile j+1's scores in two halves, each reduced while tile j's exponentials run
-                auto exps_and_next_extreme = [&](auto is_max) {
-                    constexpr bool MAX = decltype(is_max)::value;
-                    uint32_t tr[64];
-                    ptx::tmem_ld32(ts1, *reinterpret_cast<uint32_t(*)[32]>(&tr[0]));
-                    ptx::tmem_ld32(ts1 + 32, *reinterpret_cast<uint32_t(*)[32]>(&tr[32]));
-                    exp_range(std::false_type{}, I0{}, I16{});
-                    ptx::tmem_wait_ld();
-                    float t[64];
-#pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        t[i] = __uint_as_float(tr[i]);
-                    exp_range(std::false_type{}, I16{}, I32{});
-                    const float ea = row_extreme<MAX, 64>(t);
-                    ptx::tmem_ld32(ts1 + 64, *reinterpret_cast<uint32_t(*)[32]>(&tr[0]));
-                    ptx::tmem_ld32(ts1 + 96, *reinterpret_cast<uint32_t(*)[32]>(&tr[32]));
-                    exp_range(std::false_type{}, I32{}, I48{});
-                    ptx::tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        t[i] = __uint_as_float(tr[i]);
-                    exp_range(std::false_type{}, I48{}, I64{});
-                    const float eb = row_extreme<MAX, 64>(t);
-                    mx_next = MAX ? fmaxf(ea, eb) : fminf(ea, eb);
-                };
-                if (c >= 0.f)
-                    exps_and_next_extreme(std::true_type{});
-                else
-                    exps_and_next_extreme(std::false_type{});
-                have_mx = true;
-                s_seen = true;
-            } else {
-                if (tail)
-                    exp_range(std::true_type{}, I0{}, I64{});
-                else
-                    exp_range(std::false_type{}, I0{}, I64{});
-                // Poll S_{j+1}'s barrier now, so the answer returns while P_j is stored
-                // and handed off (no parity aliasing: S_j complete implies
-                // S_{j+1-NSBUF} complete, and S_{j+1+NSBUF} waits for P_{j+1}).
-                s_seen = j + 1 < n && ptx::mbar_test_wait(s_full0 + 8u * ((j + 1) % NB), ((j + 1) / NB) & 1);
-            }
+            if (tail)
+                exp_tile(std::true_type{});
+            else
+                exp_tile(std::false_type{});
+            // Poll S_{j+1}'s barrier now, so the answer returns while P_j is stored
+            // and handed off (no parity aliasing: S_j complete implies
+            // S_{j+1-NSBUF} complete, and S_{j+1+NSBUF} waits for P_{j+1}).
+            s_seen = j + 1 < n && ptx::mbar_test_wait(s_full0 + 8u * ((j + 1) % NB), ((j + 1) / NB) & 1);
             float sum0, sum1, sum2, sum3;
             ptx::f2_unpack(sum01, sum0, sum1);
             ptx::f2_unpack(sum23, sum2, sum3);

@@ -289,28 +289,3 @@ def test_persistent_pair_kernel_matches_the_per_unit_launch_bit_for_bit():
         sdp.set_debug_flags(old)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
-
-DEBUG_NO_LOOKAHEAD = 256
-
-
-@pytest.mark.parametrize("w", [
-    Workload("look_gqa4_fp16", 1, 8, 2, 1000, 2000, 128, "fp16", seed=81),
-    Workload("look_mha_bf16", 2, 2, 2, 384, 1024, 128, "bf16", seed=82),
-    Workload("look_causal_fp16", 1, 4, 2, 700, 700, 128, "fp16", seed=83, causal=True),
-    Workload("look_peaky_bf16", 1, 8, 2, 512, 3000, 128, "bf16", seed=84, peaky_k=True),
-    Workload("look_negscale_fp16", 1, 4, 1, 256, 900, 128, "fp16", seed=85, scale=-0.07),
-    Workload("look_decode_bf16", 4, 32, 8, 1, 5000, 128, "bf16", seed=86),
-], ids=lambda w: w.name)
-def test_next_tile_extreme_lookahead_is_bit_identical(w):
-    """The single-CTA softmax at D=128 finds the next tile's row extreme during the current tile's
-    exponentials (flag 256 turns that off): the same extreme and exponentials, so the same bits."""
-    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
-    o1, l1 = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=w.causal)
-    assert sdp.poll_status() == sdp.SDP_OK
-    old = sdp.set_debug_flags(DEBUG_NO_LOOKAHEAD)
-    try:
-        o2, l2 = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=w.causal)
-        assert sdp.poll_status() == sdp.SDP_OK
-    finally:
-        sdp.set_debug_flags(old)
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
