@@ -397,7 +397,7 @@ def launch_shape(w):
 def kernel_name(w):
     """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
     the units of each (batch, KV head) pair up (and, causal, share the query
-    tile), in its persistent form for dense non-causal launches with more
+    tile), in its persistent form for dense launches with more
     units than SMs, else the single-CTA kernel; split-KV adds the merge kernel;
     variable-length batches pair up when the group size is even; head dim 128
     always runs on single CTAs."""
@@ -421,9 +421,9 @@ def kernel_name(w):
     name = "sdp_fwd_pair_kernel" if pair else "sdp_fwd_kernel"
     if w.kv_splits != 1:
         return name + " + merge_kernel"
-    # dense, non-causal CTA-pair launches with more units than SMs run the persistent form
+    # dense CTA-pair launches with more units than SMs run the persistent form
     units = w.B * w.Hkv * G * n_qtiles
-    if pair and not w.causal and units > sms:
+    if pair and units > sms:
         return "sdp_fwd_pair_persistent_kernel"
     return name
 

@@ -1,5 +1,12 @@
-// Persistent form of the CTA-pair kernel, for dense, non-causal, unsplit
-// launches: one cluster per SM pair loops over unit pairs (c, c + C, ...).
+// Persistent form of the CTA-pair kernel, for dense, unsplit launches: one
+// cluster per SM pair loops over unit pairs. Without the causal mask every unit
+// reads all KV tiles and cluster c takes unit pairs c, c + C, c + 2C, ...
+// (C clusters). With it, unit pairs run longest first (query tile descending,
+// then batch and KV head, then the heads of a group) and round r of the walk
+// assigns its C pairs in forward order when r is even and in reverse order when
+// r is odd, so that the few tiles by which consecutive pairs shrink within a
+// round even out over the rounds: every cluster ends within about one round's
+// length difference of the others, with no scheduler state on the device.
 //
 // The per-tile protocol is the pair kernel's (see sdp_fwd_pair.cuh); what
 // changes is that nothing is set up or torn down per unit, and the next unit
@@ -61,27 +68,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t rank = ptx::cluster_ctarank();
     const bool leader = (rank == 0);
 
-    // Units as in the pair kernel (head-in-group fastest, then query tile, then
-    // (batch, KV head)); cluster c takes unit pairs c, c + C, c + 2C, ...
+    // Unit pairs: without the causal mask as in the pair kernel (head-in-group
+    // fastest, then query tile, then (batch, KV head)); with it, query tile
+    // descending outermost, then (batch, KV head), then head-in-group, so that the
+    // walk below takes them longest first (a causal unit of query tile qt reads
+    // qt + 1 KV tiles). Both units of a pair share the query tile (the group size
+    // is even) and so the tile count.
     const int n_pairs = p.planes_q * p.n_qtiles / 2;
     const int n_clusters = static_cast<int>(gridDim.x) / 2;
     const int cid = static_cast<int>(blockIdx.x) / 2;
-    const int n_it = cid < n_pairs ? (n_pairs - cid + n_clusters - 1) / n_clusters : 0;
-    const int n = p.n_kvtiles;  // every unit reads all KV tiles
+    const bool snake = p.causal != 0;
+    int n_it;
+    if (!snake) {
+        n_it = cid < n_pairs ? (n_pairs - cid + n_clusters - 1) / n_clusters : 0;
+    } else {
+        const int full = n_pairs / n_clusters, rem = n_pairs % n_clusters;
+        const bool in_last = rem > 0 && ((full & 1) == 0 ? cid < rem : cid >= n_clusters - rem);
+        n_it = full + (in_last ? 1 : 0);
+    }
     struct Unit {
-        int z_q, z_kv, q0;
+        int z_q, z_kv, q0, n;  // n: KV tiles the unit reads
     };
     auto unit_of = [&](int it) {
-        int u = 2 * (cid + it * n_clusters) + static_cast<int>(rank);
+        const int pos = (snake && (it & 1)) ? n_clusters - 1 - cid : cid;
+        int u = 2 * (it * n_clusters + pos) + static_cast<int>(rank);
         const int hi = u % p.G;
         u /= p.G;
-        const int qt = u % p.n_qtiles;
-        const int bg = u / p.n_qtiles;
+        int qt, bg;
+        if (snake) {
+            const int n_bg = p.planes_q / p.G;  // batch x KV heads
+            bg = u % n_bg;
+            qt = p.n_qtiles - 1 - u / n_bg;
+        } else {
+            qt = u % p.n_qtiles;
+            bg = u / p.n_qtiles;
+        }
         const int b = bg / p.Hkv;
         const int g = bg - b * p.Hkv;
-        return Unit{b * p.Hq + g * p.G + hi, bg, qt * L::BM};
+        const int n_kv = p.causal ? min(p.n_kvtiles, qt + 1) : p.n_kvtiles;
+        return Unit{b * p.Hq + g * p.G + hi, bg, qt * L::BM, n_kv};
     };
-    if (n_it == 0 || n <= 0)
+    if (n_it == 0)
         return;  // uniform across the cluster: both CTAs have the same cid
 
     if (threadIdx.x == 0) {
@@ -171,6 +198,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
                     ptx::tma_load_3d_pair_w(s_q + c * L::Q_BOX_BYTES, &tm_q, q_full_l, c * 64, un.q0, un.z_q);
+                const int n = un.n;
                 ok = load_k(0);
                 for (int j = 0; ok && j < n; ++j) {
                     if (j + 1 < n)
@@ -191,6 +219,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             for (int it = 0; ok && it < n_it; ++it) {
                 if (!(ok = __all_sync(0xffffffffu, wait_bounded(q_full, it & 1, cx, SITE_Q_FULL))))
                     break;
+                const int n = unit_of(it).n;
                 for (int t = 0; ok && t < n; ++t) {
                     const int gt = g0 + t;
                     const int pos = pos0 + pos_k<1>(t);
@@ -235,6 +264,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             int g0 = 0, pos0 = 0;
             for (int it = 0; ok && it < n_it; ++it) {
+                const int n = unit_of(it).n;
                 for (int j = 0; ok && j < n; ++j) {
                     const int gj = g0 + j;
                     const int buf = gj % NB;
@@ -298,6 +328,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         int g0 = 0;
         for (int it = 0; ok && it < n_it; ++it) {
             const Unit un = unit_of(it);
+            const int n = un.n;
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
                 const int gj = g0 + j;
@@ -318,9 +349,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 for (int i = 0; i < 128; ++i)
                     s[i] = __uint_as_float(sr[i]);
 
-                // keys of this tile the row sees (>= 1); only the ragged last tile masks
-                const int valid = p.Skv - j * L::BN;
-                const bool tail = valid < L::BN;  // the same for every row
+                // keys of this tile the row sees (>= 1): all < Skv, and (causal) <= the row
+                // itself; only the ragged last tile or a causal diagonal takes the masked path
+                const int valid = (p.causal ? min(p.Skv, un.q0 + row + 1) : p.Skv) - j * L::BN;
+                const bool tail = __any_sync(0xffffffffu, valid < L::BN);
                 if (tail) {
 #pragma unroll
                     for (int i = 1; i < 128; ++i)
@@ -513,13 +545,13 @@ cudaError_t launch_sdp_fwd_pair_persistent(const CUtensorMap &q, const CUtensorM
     return cudaGetLastError();
 }
 
-// The persistent form serves dense, non-causal, unsplit launches with more unit
-// pairs than SM pairs (otherwise each cluster would run one unit anyway).
+// The persistent form serves dense, unsplit launches (causal or not) with more
+// unit pairs than SM pairs (otherwise each cluster would run one unit anyway).
 inline bool use_persistent(const KernelParams &p, int grid)
 {
     if (p.debug_flags & DEBUG_NO_PERSIST)
         return false;
-    return !p.causal && p.cu_q == nullptr && p.kv_splits == 1 && p.o != nullptr && p.num_sms > 0 && grid > p.num_sms;
+    return p.cu_q == nullptr && p.kv_splits == 1 && p.o != nullptr && p.num_sms > 0 && grid > p.num_sms;
 }
 
 }  // namespace sdp

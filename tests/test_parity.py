@@ -289,3 +289,30 @@ def test_persistent_pair_kernel_matches_the_per_unit_launch_bit_for_bit():
         sdp.set_debug_flags(old)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
+
+
+@pytest.mark.parametrize("w", [
+    # 160 causal units at D=256, two heads per group: the persistent CTA-pair kernel, units of 1 to 20 KV tiles
+    Workload("persist_causal_fp16", 1, 8, 2, 2560, 2560, 256, "fp16", seed=87, causal=True),
+    # more query rows than keys: the late units all read the 8 KV tiles, ragged last tile
+    Workload("persist_causal_sq_gt_skv_bf16", 1, 8, 2, 2560, 1000, 256, "bf16", seed=88, causal=True),
+], ids=lambda w: w.name)
+def test_persistent_pair_kernel_causal_every_row(w):
+    """Causal launches with more units than SMs run the persistent CTA-pair kernel: unit pairs of
+    different lengths, longest first, walked in alternating directions; the diagonal tile of every
+    unit is masked per row."""
+    check_full(w)
+
+
+def test_persistent_pair_kernel_causal_matches_the_per_unit_launch_bit_for_bit():
+    w = Workload("persist_causal_eq", 1, 8, 2, 2560, 3000, 256, "fp16", seed=89, causal=True)
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    o1, l1 = sdp.sdp_fwd(q, k, v, causal=True)
+    assert sdp.poll_status() == sdp.SDP_OK
+    old = sdp.set_debug_flags(DEBUG_NO_PERSIST)
+    try:
+        o2, l2 = sdp.sdp_fwd(q, k, v, causal=True)
+        assert sdp.poll_status() == sdp.SDP_OK
+    finally:
+        sdp.set_debug_flags(old)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

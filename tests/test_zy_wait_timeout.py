@@ -35,14 +35,16 @@ def _built():
     (DEBUG_NO_LOADS, Workload("timeout_persist", 1, 8, 2, 2560, 384, 256, "fp16", seed=92)),
     # the two-tile CTA-pair kernel at D=128 (debug flag 128 forces it below one wave)
     (DEBUG_NO_LOADS | 128, Workload("timeout_pair2", 1, 4, 2, 256, 384, 128, "bf16", seed=93)),
-], ids=["cta_pair", "single_cta", "persistent_pair", "two_tile_pair"])
+    # 160 causal units of a dense D=256 launch: the persistent CTA-pair kernel's causal walk
+    (DEBUG_NO_LOADS, Workload("timeout_persist_causal", 1, 8, 2, 2560, 2560, 256, "fp16", seed=94, causal=True)),
+], ids=["cta_pair", "single_cta", "persistent_pair", "two_tile_pair", "persistent_causal"])
 def test_wait_timeout_is_reported_and_the_context_survives(flags, w):
     q, k, v = (t.cuda() for t in workloads.make_inputs(w))
     assert sdp.poll_status() == sdp.SDP_OK
     old_ms = sdp.set_wait_timeout_ms(50)
     old_flags = sdp.set_debug_flags(flags)
     try:
-        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale)
+        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=w.causal)
         assert sdp.poll_status() == sdp.SDP_ERR_DEVICE_TIMEOUT
         site = sdp.last_status_detail() & 0xFF
         assert 1 <= site <= 6, hex(sdp.last_status_detail())
@@ -51,7 +53,8 @@ def test_wait_timeout_is_reported_and_the_context_survives(flags, w):
         sdp.set_wait_timeout_ms(old_ms)
     # the status word was cleared and the device still computes correctly
     assert sdp.poll_status() == sdp.SDP_OK
-    o, lse = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale)
+    o, lse = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=w.causal)
     assert sdp.poll_status() == sdp.SDP_OK
-    ref_o, ref_l = oracle.sdp_fwd(q.cpu(), k.cpu(), v.cpu(), ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale)
+    ref_o, ref_l = oracle.sdp_fwd(q.cpu(), k.cpu(), v.cpu(), ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale,
+                                  causal=w.causal)
     assert_within(compare(o, lse, ref_o, ref_l, w.dtype), w.dtype)
