@@ -38,6 +38,9 @@ struct KernelParams {
     // Host-side facts of the launching device (not read by the kernels): its
     // SM count, cached per device so that a launch makes no attribute query.
     int num_sms;
+    // Units of the launch (the per-unit grid: one CTA per unit); set by the
+    // persistent launcher, whose grid is smaller.
+    int units;
 };
 
 // Sequences per batch up to which causal variable-length launches use the compact

@@ -233,3 +233,51 @@ def test_full_size_batches_sampled(name):
     st = compare(np.concatenate(got_o), np.concatenate(got_l), np.concatenate(ref_o), np.concatenate(ref_l),
                  w.dtype)
     assert_within(st, w.dtype)
+
+
+DEBUG_NO_PERSIST = 16
+
+# Causal batches at D=256 with an even group size and more units than SMs: the persistent
+# CTA-pair kernel (unit pairs longest first, walked in alternating directions), with empty and
+# key-less sequences, ragged tails, more keys than queries and the reverse. (The same batches
+# without the causal mask run on the per-unit CTA-pair kernel.)
+PAIRED = [VarlenWorkload(f"pairs_{'causal' if causal else 'full'}_{dt}", (0, 700, 3, 1100, 129, 40, 1),
+                         (10, 650, 0, 1200, 260, 40, 0), 16, 4, 256, dt, seed=96 + causal, causal=causal)
+          for dt in ("fp16", "bf16") for causal in (False, True)]
+PERSIST = [w for w in PAIRED if w.causal]
+
+
+@pytest.mark.parametrize("w", PAIRED, ids=lambda w: w.name)
+def test_paired_batches_with_many_units_every_row(w):
+    check_every_row(w)
+
+
+@pytest.mark.parametrize("flags", [DEBUG_NO_PERSIST, DEBUG_FULL_VARLEN_GRID], ids=["per_unit", "full_grid"])
+@pytest.mark.parametrize("w", PERSIST, ids=lambda w: w.name)
+def test_persistent_pair_kernel_matches_other_launches_bit_for_bit(w, flags):
+    """The persistent walk changes the schedule, not the arithmetic: the same bits as one unit pair
+    per cluster (flag 16), and on the full grid of the longest sequence's tiles (flag 32)."""
+    q, k, v = workloads.make_varlen_inputs(w)
+    o, lse = run(w, q, k, v)
+    old = sdp.set_debug_flags(flags)
+    try:
+        o2, l2 = run(w, q, k, v)
+    finally:
+        sdp.set_debug_flags(old)
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
+
+
+def test_bad_offsets_on_the_persistent_kernel():
+    dev = torch.device("cuda")
+    w = VarlenWorkload("bad256", (1000, 1200), (1000, 1200), 16, 2, 256, "fp16", seed=98, causal=True)
+    q, k, v = (t.to(dev) for t in workloads.make_varlen_inputs(w))
+    good_q = torch.from_numpy(w.cu_q).to(dev)
+    good_k = torch.from_numpy(w.cu_k).to(dev)
+    bad_k = torch.tensor([0, 1000, 9999], dtype=torch.int32, device=dev)  # past total_k
+    o = torch.zeros_like(q)
+    sdp.sdp_fwd_varlen(q, k, v, good_q, bad_k, 1200, out=o, causal=True)
+    assert sdp.poll_status() == sdp.SDP_ERR_BAD_SEQLENS
+    assert sdp.last_status_detail() & 0xFF == 7
+    o, lse = sdp.sdp_fwd_varlen(q, k, v, good_q, good_k, 1200, causal=True)
+    assert sdp.poll_status() == sdp.SDP_OK
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()

@@ -58,3 +58,26 @@ def test_wait_timeout_is_reported_and_the_context_survives(flags, w):
     ref_o, ref_l = oracle.sdp_fwd(q.cpu(), k.cpu(), v.cpu(), ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale,
                                   causal=w.causal)
     assert_within(compare(o, lse, ref_o, ref_l, w.dtype), w.dtype)
+
+
+def test_varlen_persistent_wait_timeout_is_reported():
+    """The persistent CTA-pair kernel on a causal variable-length batch (16 heads over 4 KV heads at
+    D=256, 304 units): every wait runs out, the status says so, and the next call is right."""
+    from gqa_flash_attention_gb300.workloads import VarlenWorkload
+    w = VarlenWorkload("timeout_varlen", (1000, 1200), (1000, 1200), 16, 4, 256, "fp16", seed=95, causal=True)
+    q, k, v = (t.cuda() for t in workloads.make_varlen_inputs(w))
+    cq, ck = torch.from_numpy(w.cu_q).cuda(), torch.from_numpy(w.cu_k).cuda()
+    assert sdp.poll_status() == sdp.SDP_OK
+    old_ms = sdp.set_wait_timeout_ms(50)
+    old_flags = sdp.set_debug_flags(DEBUG_NO_LOADS)
+    try:
+        sdp.sdp_fwd_varlen(q, k, v, cq, ck, w.max_q, scale=w.softmax_scale, causal=True)
+        assert sdp.poll_status() == sdp.SDP_ERR_DEVICE_TIMEOUT
+    finally:
+        sdp.set_debug_flags(old_flags)
+        sdp.set_wait_timeout_ms(old_ms)
+    o, lse = sdp.sdp_fwd_varlen(q, k, v, cq, ck, w.max_q, scale=w.softmax_scale, causal=True)
+    assert sdp.poll_status() == sdp.SDP_OK
+    ref_o, ref_l = oracle.sdp_fwd_varlen(q.cpu(), k.cpu(), v.cpu(), ORACLE_DTYPE[w.dtype], w.cu_q, w.cu_k,
+                                         w.softmax_scale, causal=True)
+    assert_within(compare(o, lse, ref_o, ref_l, w.dtype), w.dtype)
