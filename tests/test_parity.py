@@ -316,3 +316,4 @@ def test_persistent_pair_kernel_causal_matches_the_per_unit_launch_bit_for_bit()
     finally:
         sdp.set_debug_flags(old)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+

@@ -248,7 +248,7 @@ PERSIST = [w for w in PAIRED if w.causal]
 
 
 @pytest.mark.parametrize("w", PAIRED, ids=lambda w: w.name)
-def test_paired_batches_with_many_units_every_row(w):
+def test_batches_with_many_units_every_row(w):
     check_every_row(w)
 
 
