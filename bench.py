@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--override", nargs="*", default=[], metavar="FIELD=VALUE",
                     help="change fields of a dense workload (B, Hq, Hkv, Sq, Skv): a smaller case of the same "
                          "kernel, e.g. for a multi-pass ncu capture; the workload name gets the changes appended")
+    ap.add_argument("--debug-flags", type=int, default=0,
+                    help="the library's test hooks (sdp_set_debug_flags), e.g. 128 for the opt-in two-tile "
+                         "kernel at head dim 128; 0 (the default) runs what sdp_fwd picks")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="replay each step from a CUDA graph (auto: for the split-KV decode workloads, whose "
                          "steps are shorter than the host's per-call work)")
@@ -394,7 +397,7 @@ def launch_shape(w):
     return w.Sq, G
 
 
-def kernel_name(w):
+def kernel_name(w, debug_flags=0):
     """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
     the units of each (batch, KV head) pair up (and, causal, share the query
     tile), in its persistent form for dense launches with more
@@ -406,11 +409,11 @@ def kernel_name(w):
         # dense, non-causal launches whose two-tile units pair up and fill a wave of CTAs run the
         # two-tile CTA-pair kernel; the rest the single-CTA kernel
         name = "sdp_fwd_kernel"
-        if PAIR2_BY_DEFAULT and not is_varlen(w) and not w.causal:
+        if (PAIR2_BY_DEFAULT or debug_flags & 128) and not is_varlen(w) and not w.causal:
             sq, G = launch_shape(w)
             n_qpairs = ((sq + 127) // 128 + 1) // 2
             splits = max(1, w.kv_splits)
-            if (n_qpairs * G) % 2 == 0 and w.B * w.Hkv * G * n_qpairs * splits >= sms:
+            if (n_qpairs * G) % 2 == 0 and (w.B * w.Hkv * G * n_qpairs * splits >= sms or debug_flags & 128):
                 name = "sdp_fwd_pair2_kernel"
         return name + " + merge_kernel" if getattr(w, "kv_splits", 1) != 1 else name
     if is_varlen(w):
@@ -465,6 +468,7 @@ def ours_arm(args, w):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     sdp.lib()
+    sdp.set_debug_flags(args.debug_flags)
 
     q_h, k_h, v_h = host_inputs(w)
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
@@ -631,7 +635,7 @@ def ours_arm(args, w):
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
                     "traffic": load_traffic(w.name), "peak_source": f"{hbm_src} HBM copy bandwidth",
                     "algorithmic_bytes": w.hbm_bytes(), "tflops": tflops}
-    roofline.update({"kernel": kernel_name(w), "launch_ms_median": statistics.median(per_launch_ms),
+    roofline.update({"kernel": kernel_name(w, args.debug_flags), "launch_ms_median": statistics.median(per_launch_ms),
                      "flop_per_byte": intensity})
     if roofline["bound"] == "tensor":
         roofline.update({"peak_datasheet": DATASHEET_TFLOPS, "frac_datasheet": tflops / DATASHEET_TFLOPS,
@@ -653,6 +657,8 @@ def ours_arm(args, w):
 
     cfg = config_of(w, world)
     cfg["cuda_graph"] = use_graph
+    if args.debug_flags:
+        cfg["debug_flags"] = args.debug_flags
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "latency_us_per_step": 1000 * ms_per_step, "higher_is_better": True,
