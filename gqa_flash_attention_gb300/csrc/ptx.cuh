@@ -100,7 +100,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until every committed bulk store has finished READING its shared-memory source: the
+// staging tile may then be reused or the CTA may exit (the global writes complete on their own
+// and are visible to any later kernel).
+__device__ __forceinline__ void bulk_wait_group_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // Order this thread's generic-proxy shared-memory writes before later async-proxy reads.
 __device__ __forceinline__ void fence_proxy_async_smem()

@@ -168,6 +168,32 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// Epilogue read-out of one accumulator row: O's D fp32 columns leave tensor memory GROUP
+// chunks of 32 at a time behind one wait (one load latency per group instead of per chunk;
+// the softmax arrays are dead here, so the 32 * GROUP values fit in registers), are scaled
+// by 1/l and rounded to 16 bits, and each chunk's 16 packed words go to emit(chunk, words).
+template <int D, bool BF16, int GROUP, typename Emit>
+__device__ __forceinline__ void drain_o_row(uint32_t t_o, float inv_l, Emit &&emit)
+{
+    static_assert((D / 32) % GROUP == 0, "chunk groups");
+#pragma unroll 1
+    for (int c0 = 0; c0 < D / 32; c0 += GROUP) {
+        uint32_t o[GROUP][32];
+#pragma unroll
+        for (int g = 0; g < GROUP; ++g)
+            ptx::tmem_ld32(t_o + 32 * (c0 + g), o[g]);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int g = 0; g < GROUP; ++g) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = pack2<BF16>(__uint_as_float(o[g][2 * i]) * inv_l, __uint_as_float(o[g][2 * i + 1]) * inv_l);
+            emit(c0 + g, pk);
+        }
+    }
+}
+
 // Geometry of one unit's sequence: where its Q/O rows and K/V rows start in
 // the (token) row coordinate, and how many of each it has. Without a
 // variable-length batch it is the whole plane.
@@ -777,16 +803,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (ok) {
             ptx::tc_fence_after();
-            const float inv_l = 1.f / l;
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                ptx::tmem_ld32(t_o + 32 * cc, o);
-                ptx::tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            drain_o_row<D, BF16, 4>(t_o, 1.f / l, [&](int cc, const uint32_t (&pk)[16]) {
                 if (direct_store) {
                     // the rows of this sequence only, 64 bytes per row per step
                     if (q0 + row < sg.sq) {
@@ -797,7 +814,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int v = 0; v < 4; ++v)
                             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                     }
-                    continue;
+                    return;
                 }
                 // 32 columns = four 16-byte units of row `row` in box cc/2, 128-byte swizzled.
                 const uint32_t row_addr = s_q + (cc >> 1) * L::BOX_BYTES + row * 128;
@@ -807,7 +824,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     st_shared_v4(row_addr + ((unit ^ static_cast<uint32_t>(row & 7)) << 4), pk[4 * v], pk[4 * v + 1],
                                  pk[4 * v + 2], pk[4 * v + 3]);
                 }
-            }
+            });
             if (p.lse != nullptr && q0 + row < sg.sq)
                 p.lse[static_cast<size_t>(z_out) * p.Sq + q_row + row] = (m_used + ptx::lg2(l)) * LN2;
             ptx::fence_proxy_async_smem();
@@ -818,7 +835,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int c2 = 0; c2 < D / L::BOX_COLS; ++c2)
                 ptx::tma_store_3d(&tm_o, s_q + c2 * L::BOX_BYTES, c2 * L::BOX_COLS, q_row, z_out);
             ptx::bulk_commit_group();
-            ptx::bulk_wait_group_all();
+            ptx::bulk_wait_group_read_all();
         }
     }
 

@@ -564,16 +564,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             // o_done of the last PV implies every S MMA (which read both CTAs' Q) completed,
             // so the Q tile can be reused as the O staging tile.
             ptx::tc_fence_after();
-            const float inv_l = 1.f / l;
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                ptx::tmem_ld32(t_o + 32 * cc, o);
-                ptx::tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            drain_o_row<D, BF16, 4>(t_o, 1.f / l, [&](int cc, const uint32_t (&pk)[16]) {
                 if (direct_store) {
                     // the rows of this sequence only, 64 bytes per row per step
                     if (q0 + row < sg.sq) {
@@ -584,7 +575,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                         for (int v = 0; v < 4; ++v)
                             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                     }
-                    continue;
+                    return;
                 }
                 const uint32_t row_addr = s_q + (cc >> 1) * L::Q_BOX_BYTES + row * 128;
 #pragma unroll
@@ -593,7 +584,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     st_shared_v4(row_addr + ((unit ^ static_cast<uint32_t>(row & 7)) << 4), pk[4 * v], pk[4 * v + 1],
                                  pk[4 * v + 2], pk[4 * v + 3]);
                 }
-            }
+            });
             if (p.lse != nullptr && q0 + row < sg.sq)
                 p.lse[static_cast<size_t>(z_out) * p.Sq + q_row + row] = (m_used + ptx::lg2(l)) * LN2;
             ptx::fence_proxy_async_smem();
@@ -604,7 +595,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             for (int c2 = 0; c2 < D / 64; ++c2)
                 ptx::tma_store_3d(&tm_o, s_q + c2 * L::Q_BOX_BYTES, c2 * 64, q_row, z_out);
             ptx::bulk_commit_group();
-            ptx::bulk_wait_group_all();
+            ptx::bulk_wait_group_read_all();
         }
     }
 

@@ -490,16 +490,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair2Layout::THREADS
             // PV_x(n-1) complete implies every S_x MMA (which read both CTAs' Q_x) completed,
             // so Q_x's shared memory can hold the O staging tile.
             ptx::tc_fence_after();
-            const float inv_l = 1.f / l;
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                ptx::tmem_ld32(t_o + 32 * cc, o);
-                ptx::tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            // two chunks per wait: 384 threads leave at most 168 registers a thread
+            drain_o_row<D, BF16, 2>(t_o, 1.f / l, [&](int cc, const uint32_t (&pk)[16]) {
                 // 32 columns = four 16-byte units of row `row` in box cc/2, 128-byte swizzled
                 const uint32_t row_addr = s_stage + (cc >> 1) * L::Q_BOX_BYTES + row * 128;
 #pragma unroll
@@ -508,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair2Layout::THREADS
                     st_shared_v4(row_addr + ((unit ^ static_cast<uint32_t>(row & 7)) << 4), pk[4 * v], pk[4 * v + 1],
                                  pk[4 * v + 2], pk[4 * v + 3]);
                 }
-            }
+            });
             if (p.lse != nullptr && tile_row0 + row < p.Sq)
                 p.lse[static_cast<size_t>(z_out) * p.Sq + tile_row0 + row] = (m_used + ptx::lg2(l)) * LN2;
             ptx::fence_proxy_async_smem();
@@ -520,7 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Pair2Layout::THREADS
             for (int c2 = 0; c2 < D / 64; ++c2)
                 ptx::tma_store_3d(&tm_o, s_stage + c2 * L::Q_BOX_BYTES, c2 * 64, tile_row0, z_out);
             ptx::bulk_commit_group();
-            ptx::bulk_wait_group_all();
+            ptx::bulk_wait_group_read_all();
         }
     }
 

@@ -577,24 +577,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     break;
             }
             ptx::tc_fence_after();
-            const float inv_l = 1.f / l;
             const bool row_ok = un.q0 + row < un.sq;
             uint4 *dst = o_row(un);
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                ptx::tmem_ld32(t_o + 32 * cc, o);
-                ptx::tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            // One chunk per wait and O released after the stores: the next unit's S MMAs run
+            // meanwhile, and four-chunk loads with an earlier release measured 6 % slower here.
+            drain_o_row<D, BF16, 1>(t_o, 1.f / l, [&](int cc, const uint32_t (&pk)[16]) {
                 if (row_ok) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
                         dst[4 * cc + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                 }
-            }
+            });
             hand_over(o_free);
             if (p.lse != nullptr && row_ok)
                 p.lse[static_cast<size_t>(un.z_q) * p.Sq + un.q_row + row] = (m_used + ptx::lg2(l)) * LN2;

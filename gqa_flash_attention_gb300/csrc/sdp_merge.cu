@@ -24,6 +24,17 @@ namespace {
 
 constexpr int kWarpsPerBlock = 4;
 
+// With up to NP parts (a template bound of 8, 16 or 32; 0 for none) every load
+// of a row (the part rows and lane p's part LSE) is issued at once: the split-KV
+// merge of a decode step has few rows and is bound by that one round trip (about
+// 0.8 us to L2 on this GPU, so a row read in five trips costs four times as
+// much). The bound sizes the row's register array, so a caller picks the
+// smallest one that holds its P: an HBM-bound merge of many rows then keeps its
+// occupancy. Beyond the bound, the part LSEs are read once (lane p holds part
+// p's while P <= 32) and the part rows MAX_IN_FLIGHT at a time. The arithmetic
+// does not depend on the bound.
+constexpr int MAX_IN_FLIGHT = 8;
+
 template <bool BF16>
 __device__ __forceinline__ float2 unpack2(uint32_t u)
 {
@@ -76,27 +87,15 @@ __device__ __forceinline__ void store_row(uint16_t *o, float *lse, long long r, 
         lse[r] = lse_r;
 }
 
-// One warp per row. With up to kFastParts parts every load of a row (the
-// part rows and lane p's part LSE) is issued at once: the split-KV merge of a
-// decode step has few rows and is bound by that one round trip. Beyond that,
-// the part LSEs are read once (lane p holds part p's while P <= 32) and the
-// part rows kMaxInFlight at a time; the context-parallel merge of long
-// sequences is bound by HBM bandwidth either way.
-constexpr int kMaxInFlight = 8;
-constexpr int kFastParts = 16;  // up to this many parts, one round trip per row
-
-template <int D, bool BF16>
-__global__ void __launch_bounds__(32 * kWarpsPerBlock)
-    merge_kernel(const uint16_t *__restrict__ o_parts, const float *__restrict__ lse_parts, int P, long long rows,
-                 uint16_t *__restrict__ o, float *__restrict__ lse)
+// Row r of P parts ([P, rows, D] 16-bit O and [P, rows] fp32 LSE) into o / lse;
+// called by all 32 lanes of a warp.
+template <int D, bool BF16, int NP>
+__device__ __forceinline__ void merge_row(const uint16_t *__restrict__ o_parts, const float *__restrict__ lse_parts,
+                                          int P, long long rows, long long r, int lane, uint16_t *__restrict__ o,
+                                          float *__restrict__ lse)
 {
     constexpr int W = D / 64;  // 2 (8-byte loads) at D=128, 4 (16-byte loads) at D=256
     using Vec = typename std::conditional<W == 4, uint4, uint2>::type;
-    const int lane = threadIdx.x & 31;
-    const long long r = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-    if (r >= rows)
-        return;
-
     const Vec *src = reinterpret_cast<const Vec *>(o_parts) + r * 32 + lane;
     const long long part_stride = rows * 32;  // in Vec units
     float acc[2 * W];
@@ -104,33 +103,33 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     for (int i = 0; i < 2 * W; ++i)
         acc[i] = 0.f;
 
-    if (P <= kFastParts) {
-        // Few parts (the split-KV merge of a decode step): every load of the
-        // row is issued before the reductions, one memory round trip in all.
-        Vec v[kFastParts];
+    if constexpr (NP > 0) {
+        if (P <= NP) {
+            Vec v[NP];
 #pragma unroll
-        for (int u = 0; u < kFastParts; ++u)
-            if (u < P)
-                v[u] = __ldg(src + static_cast<long long>(u) * part_stride);
-        const float l = lane < P ? __ldg(lse_parts + static_cast<long long>(lane) * rows + r) : -INFINITY;
-        float m = l;
+            for (int u = 0; u < NP; ++u)
+                if (u < P)
+                    v[u] = __ldg(src + static_cast<long long>(u) * part_stride);
+            const float l = lane < P ? __ldg(lse_parts + static_cast<long long>(lane) * rows + r) : -INFINITY;
+            float m = l;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        const float e = lane < P ? expf(l - m) : 0.f;
-        float sum = e;
+            for (int off = 16; off > 0; off >>= 1)
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            const float e = lane < P ? expf(l - m) : 0.f;
+            float sum = e;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        const float w_l = e / sum;
+            for (int off = 16; off > 0; off >>= 1)
+                sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            const float w_l = e / sum;
 #pragma unroll
-        for (int u = 0; u < kFastParts; ++u) {
-            const float w = __shfl_sync(0xffffffffu, w_l, u);
-            if (u < P)
-                accumulate<D, BF16>(acc, reinterpret_cast<const uint32_t *>(&v[u]), w);
+            for (int u = 0; u < NP; ++u) {
+                const float w = __shfl_sync(0xffffffffu, w_l, u);
+                if (u < P)
+                    accumulate<D, BF16>(acc, reinterpret_cast<const uint32_t *>(&v[u]), w);
+            }
+            store_row<D, BF16>(o, lse, r, lane, acc, m + logf(sum));
+            return;
         }
-        store_row<D, BF16>(o, lse, r, lane, acc, m + logf(sum));
-        return;
     }
 
     // Row log-sum-exp over the parts: max, then sum of exp relative to it.
@@ -159,14 +158,14 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
                                   : (pl < P ? expf(__ldg(lse_parts + static_cast<long long>(pl) * rows + r) - lse_r)
                                             : 0.f);
         const int pend = min(32, P - p0);
-        for (int q = 0; q < pend; q += kMaxInFlight) {
-            Vec v[kMaxInFlight];
+        for (int q = 0; q < pend; q += MAX_IN_FLIGHT) {
+            Vec v[MAX_IN_FLIGHT];
 #pragma unroll
-            for (int u = 0; u < kMaxInFlight; ++u)
+            for (int u = 0; u < MAX_IN_FLIGHT; ++u)
                 if (q + u < pend)
                     v[u] = __ldg(src + static_cast<long long>(p0 + q + u) * part_stride);
 #pragma unroll
-            for (int u = 0; u < kMaxInFlight; ++u) {
+            for (int u = 0; u < MAX_IN_FLIGHT; ++u) {
                 const float w = __shfl_sync(0xffffffffu, w_l, (q + u) & 31);
                 if (q + u < pend)
                     accumulate<D, BF16>(acc, reinterpret_cast<const uint32_t *>(&v[u]), w);
@@ -176,13 +175,34 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     store_row<D, BF16>(o, lse, r, lane, acc, lse_r);
 }
 
+// One instantiation per all-in-flight bound NP (8, 16, 32; 0: none), so that each
+// has the registers (and occupancy) of its own row array.
+template <int D, bool BF16, int NP>
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+    merge_kernel(const uint16_t *__restrict__ o_parts, const float *__restrict__ lse_parts, int P, long long rows,
+                 uint16_t *__restrict__ o, float *__restrict__ lse)
+{
+    const long long r = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (r >= rows)
+        return;
+    merge_row<D, BF16, NP>(o_parts, lse_parts, P, rows, r, threadIdx.x & 31, o, lse);
+}
+
 template <int D, bool BF16>
 cudaError_t launch(const void *o_parts, const float *lse_parts, int P, long long rows, void *o, float *lse,
                    cudaStream_t st)
 {
-    const long long blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
-merge_kernel<D, BF16><<<static_cast<unsigned>(blocks), 32 * kWarpsPerBlock, 0, st>>>(
-        static_cast<const uint16_t *>(o_parts), lse_parts, P, rows, static_cast<uint16_t *>(o), lse);
+    const unsigned blocks = static_cast<unsigned>((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    const auto *op = static_cast<const uint16_t *>(o_parts);
+    auto *out = static_cast<uint16_t *>(o);
+    if (P <= 8)
+        merge_kernel<D, BF16, 8><<<blocks, 32 * kWarpsPerBlock, 0, st>>>(op, lse_parts, P, rows, out, lse);
+    else if (P <= 16)
+        merge_kernel<D, BF16, 16><<<blocks, 32 * kWarpsPerBlock, 0, st>>>(op, lse_parts, P, rows, out, lse);
+    else if (P <= 32)
+        merge_kernel<D, BF16, 32><<<blocks, 32 * kWarpsPerBlock, 0, st>>>(op, lse_parts, P, rows, out, lse);
+    else
+        merge_kernel<D, BF16, 0><<<blocks, 32 * kWarpsPerBlock, 0, st>>>(op, lse_parts, P, rows, out, lse);
     return cudaGetLastError();
 }
 
