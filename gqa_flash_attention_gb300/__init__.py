@@ -99,17 +99,33 @@ def _check(rc: int) -> None:
         raise SdpError(rc, msg)
 
 
+def _index(device) -> int:
+    """A CUDA device's index (a torch.device, or an int already)."""
+    if isinstance(device, int):
+        return device
+    return torch.cuda.current_device() if device.index is None else device.index
+
+
 def _on(device):
     """The device context of a call: none when `device` is already current (entering
     torch.cuda.device costs microseconds per call)."""
-    if device.index is None or device.index == torch.cuda.current_device():
+    idx = _index(device)
+    if idx == torch.cuda.current_device():
         return contextlib.nullcontext()
-    return torch.cuda.device(device)
+    return torch.cuda.device(idx)
+
+
+# The current stream's handle without building a torch.cuda.Stream object (which costs
+# microseconds per call); the public route where this build of torch lacks the query.
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream_handle(stream, device) -> int:
     if stream is None:
-        return torch.cuda.current_stream(device).cuda_stream
+        idx = _index(device)
+        if _raw_current_stream is not None:
+            return int(_raw_current_stream(idx))
+        return torch.cuda.current_stream(idx).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)
@@ -117,11 +133,11 @@ def _stream_handle(stream, device) -> int:
 
 def sdp_fwd_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
                 scale: float, dtype: int, stream: int = 0, causal: bool = False) -> int:
-    """The raw C call (sdp_fwd, or sdp_fwd_causal) with integer addresses; returns the status code."""
-    fn = lib().sdp_fwd_causal if causal else lib().sdp_fwd
-    return int(fn(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.c_void_p(o),
-                             ctypes.c_void_p(lse), int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(D),
-                             ctypes.c_float(scale), int(dtype), ctypes.c_void_p(stream)))
+    """The raw C call (sdp_fwd, or sdp_fwd_causal) with integer addresses; returns the status code.
+    (The argument types are declared on the function, so ctypes converts plain ints and floats.)"""
+    L = _lib if _lib is not None else lib()
+    fn = L.sdp_fwd_causal if causal else L.sdp_fwd
+    return fn(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, scale, dtype, stream)
 
 
 def sdp_fwd_splitkv_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: int, Hkv: int, Sq: int, Skv: int,
@@ -168,26 +184,30 @@ def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
     """
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D [B, H, S, D]")
-    if not (q.is_cuda and k.is_cuda and v.is_cuda) or not (q.device == k.device == v.device):
+    # integer device indices (get_device() is -1 off the GPU): cheaper than torch.device objects
+    dev = q.get_device()
+    if dev < 0 or k.get_device() != dev or v.get_device() != dev:
         raise ValueError("q, k, v must be CUDA tensors on one device")
-    if q.dtype not in _DTYPE_CODE or k.dtype != q.dtype or v.dtype != q.dtype:
+    dt = _DTYPE_CODE.get(q.dtype)
+    if dt is None or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("q, k, v must share one dtype, float16 or bfloat16")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
     B, Hq, Sq, D = q.shape
-    if k.shape[0] != B or k.shape[3] != D or v.shape != k.shape:
+    kshape = k.shape
+    if kshape[0] != B or kshape[3] != D or v.shape != kshape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
-    Hkv, Skv = k.shape[1], k.shape[2]
+    Hkv, Skv = kshape[1], kshape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
-    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != q.device:
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.get_device() != dev:
         raise ValueError("out must be a contiguous tensor shaped and typed like q")
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     if lse is not None and (lse.shape != (B, Hq, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous()
-                            or lse.device != q.device):
+                            or lse.get_device() != dev):
         raise ValueError("lse must be a contiguous float32 tensor [B, Hq, Sq] on q's device")
     if kv_splits != 1:
         if causal:
@@ -208,11 +228,12 @@ def sdp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | No
                                      _stream_handle(stream, q.device))
         _check(rc)
         return out, lse
-    with _on(q.device):
+    with _on(dev):
         rc = sdp_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                         0 if lse is None else lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
-                         _DTYPE_CODE[q.dtype], _stream_handle(stream, q.device), causal=causal)
-    _check(rc)
+                         0 if lse is None else lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale), dt,
+                         _stream_handle(stream, dev), causal=causal)
+    if rc != SDP_OK:
+        _check(rc)
     return out, lse
 
 
