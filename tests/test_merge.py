@@ -38,7 +38,9 @@ def random_parts(P, rows, D, dtype, seed, neg_inf_part=None):
 
 @pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
-@pytest.mark.parametrize("P,rows", [(2, 1000), (5, 37), (16, 77), (17, 50), (32, 40), (33, 29), (37, 131), (1, 64)])
+# part counts on both sides of each all-in-flight bound of the merge kernels (8, 16, 32; more: batches of 8)
+@pytest.mark.parametrize("P,rows", [(2, 1000), (5, 37), (8, 45), (9, 61), (16, 77), (17, 50), (32, 40), (33, 29),
+                                    (37, 131), (1, 64)])
 def test_merge_matches_oracle(D, dtype, P, rows):
     o_parts, lse_parts = random_parts(P, rows, D, dtype, seed=P * 1000 + rows)
     o, lse = sdp.sdp_merge(o_parts.cuda(), lse_parts.cuda())
