@@ -80,6 +80,16 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 3-D tiled prefetch of one box into L2 (no shared-memory destination, no barrier): a hint
+// that starts the box's DRAM reads early; a later tiled load of the same box finds it in L2.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // 3-D tiled load into this CTA's shared memory; completes `bytes` on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y, int z)
 {

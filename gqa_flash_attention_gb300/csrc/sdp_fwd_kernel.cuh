@@ -470,6 +470,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // A variable-length tile that ends past its sequence is stored row by row.
     const bool direct_store = varlen && q0 + L::BM > sg.sq;
 
+    // The first DRAM reads (the Q tile, K_0 and V_0, the producer's first copies, same boxes) start
+    // now, into L2, so that their latency overlaps barrier set-up and the tensor-memory allocation.
+    if (warp == 4 && lane == 0 && !(p.debug_flags & DEBUG_NO_LOADS)) {
+        const int y = sg.kv_row0 + t0 * L::BN;
+#pragma unroll
+        for (int c = 0; c < D / L::BOX_COLS; ++c) {
+            ptx::tma_prefetch_3d(&tm_q, c * L::BOX_COLS, q_row, z_q);
+            ptx::tma_prefetch_3d(&tm_k, c * L::BOX_COLS, y, z_kv);
+            ptx::tma_prefetch_3d(&tm_v, c * L::BOX_COLS, y, z_kv);
+        }
+    }
+
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
         for (int s = 0; s < NS; ++s) {

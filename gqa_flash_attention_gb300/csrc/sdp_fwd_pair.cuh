@@ -210,6 +210,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // A variable-length tile that ends past its sequence is stored row by row.
     const bool direct_store = varlen && q0 + L::BM > sg.sq;
 
+    // This CTA's first DRAM reads (its Q tile, its half of K_0 and of V_0: the producer's first copies,
+    // same boxes) start now, into L2, so that their latency overlaps barrier set-up, the tensor-memory
+    // allocation and the cluster barrier.
+    if (warp == 4 && lane == 0 && !(p.debug_flags & DEBUG_NO_LOADS)) {
+        const int y = sg.kv_row0 + t0 * L::BN;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            ptx::tma_prefetch_3d(&tm_q, c * 64, q_row, z_q);
+            ptx::tma_prefetch_3d(&tm_k, c * 64, y + 64 * static_cast<int>(rank), z_kv);
+        }
+#pragma unroll
+        for (int c = 0; c < D / 128; ++c)
+            ptx::tma_prefetch_3d(&tm_v, static_cast<int>(rank) * (D / 2) + c * 64, y, z_kv);
+    }
+
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
         for (int s = 0; s < NS; ++s) {
