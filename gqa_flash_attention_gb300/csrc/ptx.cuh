@@ -40,13 +40,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
-                 "r"(bytes)
-                 : "memory");
-}
-
 // True once the phase with the given parity has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
@@ -87,15 +80,6 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, i
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
-// 3-D tiled load into this CTA's shared memory; completes `bytes` on `bar`.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y, int z)
-{
-    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
 
@@ -146,35 +130,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16 or bf16 operands, fp32 accumulate).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 operation this thread issued before has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -266,17 +221,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
-// 3-D tiled load into this CTA's shared memory whose completion is counted on
-// a barrier that may live in the peer CTA (shared::cluster address).
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster, int x,
-                                                 int y, int z)
-{
-    asm volatile("cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
 // Executed by one warp in each CTA of the pair.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t holder_smem, uint32_t ncols)
 {
@@ -294,36 +238,6 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// Arrive once on `bar` (same offset) in both CTAs of the pair when every
-// tcgen05 operation this thread issued before has completed.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     bar),
-                 "h"(static_cast<uint16_t>(3))
-                 : "memory");
-}
-
 __device__ __forceinline__ void nanosleep_ns(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
 
 // ------------------------------------------- whole-warp issue, one lane acts
@@ -333,6 +247,7 @@ __device__ __forceinline__ void nanosleep_ns(uint32_t ns) { asm volatile("nanosl
 // predicate, it keeps pace with the tensor core. These variants are called by
 // all 32 lanes of a warp with identical operands.
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16 or bf16 operands, fp32 accumulate).
 __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate)
 {
@@ -342,6 +257,7 @@ __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint6
                  : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16.
 __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate)
 {
@@ -351,6 +267,7 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint6
                  : "memory");
 }
 
+// Arrive once on `bar` when every tcgen05 operation this thread issued before has completed.
 __device__ __forceinline__ void mma_commit_w(uint32_t bar)
 {
     asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -358,6 +275,7 @@ __device__ __forceinline__ void mma_commit_w(uint32_t bar)
                  : "memory");
 }
 
+// The CTA-pair forms (cta_group::2): one M=256 MMA over both CTAs' tensor cores, issued by the leader.
 __device__ __forceinline__ void mma_ss_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                               uint32_t accumulate)
 {
@@ -376,6 +294,8 @@ __device__ __forceinline__ void mma_ts_pair_w(uint32_t d_tmem, uint32_t a_tmem, 
                  : "memory");
 }
 
+// Arrive once on `bar` (same offset) in both CTAs of the pair when every
+// tcgen05 operation this thread issued before has completed.
 __device__ __forceinline__ void mma_commit_pair_w(uint32_t bar)
 {
     asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -385,6 +305,7 @@ __device__ __forceinline__ void mma_commit_pair_w(uint32_t bar)
                  : "memory");
 }
 
+// Arrive on `bar` and add `bytes` to the transaction count its phase waits for.
 __device__ __forceinline__ void mbar_arrive_expect_tx_w(uint32_t bar, uint32_t bytes)
 {
     asm volatile("{\n\t.reg .pred e;\n\t.reg .b64 st;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -393,6 +314,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_w(uint32_t bar, uint32_t b
                  : "memory");
 }
 
+// 3-D tiled load into this CTA's shared memory; completes its bytes on `bar`.
 __device__ __forceinline__ void tma_load_3d_w(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y, int z)
 {
     asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -402,6 +324,8 @@ __device__ __forceinline__ void tma_load_3d_w(uint32_t dst, const CUtensorMap *m
                  : "memory");
 }
 
+// 3-D tiled load into this CTA's shared memory whose completion is counted on
+// a barrier that may live in the peer CTA (shared::cluster address).
 __device__ __forceinline__ void tma_load_3d_pair_w(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster, int x,
                                                    int y, int z)
 {
@@ -498,23 +422,6 @@ __device__ __forceinline__ float lg2(float x)
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// Per-thread register limit of the executing warpgroup (all four of its warps
-// execute it): raise it by taking registers from the block's pool, or lower it
-// to return registers to the pool. The sum over warpgroups must stay within the
-// block's allocation at launch (threads x registers per thread).
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_inc()
-{
-    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_dec()
-{
-    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
