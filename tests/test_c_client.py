@@ -39,11 +39,15 @@ def test_c_client_builds_and_links():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("w", [
-    Workload("c_gqa", 1, 8, 2, 300, 500, 128, "fp16", seed=95),
-    Workload("c_bf16", 2, 4, 4, 129, 130, 256, "bf16", seed=96),
-], ids=lambda w: w.name)
-def test_c_client_matches_the_oracle(w):
+@pytest.mark.parametrize("w,mode", [
+    (Workload("c_gqa", 1, 8, 2, 300, 500, 128, "fp16", seed=95), ["fwd"]),
+    (Workload("c_bf16", 2, 4, 4, 129, 130, 256, "bf16", seed=96), ["fwd"]),
+    (Workload("c_causal", 1, 8, 2, 300, 300, 256, "fp16", seed=97, causal=True), ["causal"]),
+    (Workload("c_splitkv", 2, 16, 2, 1, 3000, 256, "fp16", seed=98), ["splitkv", "0"]),
+    (Workload("c_splitkv3", 1, 8, 4, 7, 2000, 128, "bf16", seed=99), ["splitkv", "3"]),
+    (Workload("c_noalloc", 1, 16, 1, 1, 1000, 256, "fp16", seed=100), ["noalloc"]),
+], ids=lambda x: x.name if isinstance(x, Workload) else "-".join(x))
+def test_c_client_matches_the_oracle(w, mode):
     q, k, v = workloads.make_inputs(w)
     with tempfile.TemporaryDirectory() as d:
         exe = build_client(d)
@@ -53,11 +57,11 @@ def test_c_client_matches_the_oracle(w):
                 f.write(t.contiguous().view(torch.int16).numpy().tobytes())
         dt = 1 if w.dtype == "bf16" else 0
         r = subprocess.run([exe, fin, fout, *map(str, (w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, dt)),
-                            repr(w.softmax_scale)], capture_output=True, text=True, timeout=300)
+                            repr(w.softmax_scale), *mode], capture_output=True, text=True, timeout=300)
         assert r.returncode == 0, r.stderr
         raw = open(fout, "rb").read()
     nq = q.numel()
     o = torch.from_numpy(np.frombuffer(raw[:2 * nq], dtype=np.int16).copy()).view(w.torch_dtype).view(q.shape)
     lse = torch.from_numpy(np.frombuffer(raw[2 * nq:], dtype=np.float32).copy()).view(w.B, w.Hq, w.Sq)
-    ref_o, ref_l = oracle.sdp_fwd(q, k, v, ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale)
+    ref_o, ref_l = oracle.sdp_fwd(q, k, v, ORACLE_DTYPE[w.dtype], w.shape, w.softmax_scale, causal=w.causal)
     assert_within(compare(o, lse, ref_o, ref_l, w.dtype), w.dtype)
