@@ -400,10 +400,10 @@ def launch_shape(w):
 def kernel_name(w, debug_flags=0):
     """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
     the units of each (batch, KV head) pair up (and, causal, share the query
-    tile), in its persistent form for dense launches with more
-    units than SMs, else the single-CTA kernel; split-KV adds the merge kernel;
-    variable-length batches pair up when the group size is even; head dim 128
-    always runs on single CTAs."""
+    tile), else the single-CTA kernel, each in its persistent form for dense
+    launches with more units than SMs (debug bit 4 keeps one CTA or pair per
+    unit); split-KV adds the merge kernel; variable-length batches pair up when
+    the group size is even; head dim 128 runs on single CTAs."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
     if w.D == 128:
         # dense, non-causal launches whose two-tile units pair up and fill a wave of CTAs run the
@@ -415,7 +415,13 @@ def kernel_name(w, debug_flags=0):
             splits = max(1, w.kv_splits)
             if (n_qpairs * G) % 2 == 0 and (w.B * w.Hkv * G * n_qpairs * splits >= sms or debug_flags & 128):
                 name = "sdp_fwd_pair2_kernel"
-        return name + " + merge_kernel" if getattr(w, "kv_splits", 1) != 1 else name
+        if getattr(w, "kv_splits", 1) != 1:
+            return name + " + merge_kernel"
+        if name == "sdp_fwd_kernel" and not is_varlen(w) and not debug_flags & 16:
+            sq, G = launch_shape(w)
+            if w.B * w.Hkv * G * ((sq + 127) // 128) > sms:
+                return "sdp_fwd_persist_kernel"
+        return name
     if is_varlen(w):
         return "sdp_fwd_pair_kernel" if (w.Hq // w.Hkv) % 2 == 0 else "sdp_fwd_kernel"
     sq, G = launch_shape(w)
@@ -424,10 +430,10 @@ def kernel_name(w, debug_flags=0):
     name = "sdp_fwd_pair_kernel" if pair else "sdp_fwd_kernel"
     if w.kv_splits != 1:
         return name + " + merge_kernel"
-    # dense CTA-pair launches with more units than SMs run the persistent form
+    # dense launches with more units than SMs run the persistent forms
     units = w.B * w.Hkv * G * n_qtiles
-    if pair and units > sms:
-        return "sdp_fwd_pair_persistent_kernel"
+    if units > sms and not debug_flags & 16:
+        return "sdp_fwd_pair_persistent_kernel" if pair else "sdp_fwd_persist_kernel"
     return name
 
 

@@ -349,7 +349,7 @@ def set_debug_flags(flags: int) -> int:
 
     1: the load warp issues no copies (every wait runs out: the timeout path);
     2: never the CTA-pair kernel; 4: never pack a group's query heads; 8: the
-    CTA-pair kernel at head dim 128 too; 16: one CTA pair per unit where the
+    CTA-pair kernel at head dim 128 too; 16: one CTA (pair) per unit where a
     persistent kernel would run; 32: variable-length launches on the full grid
     instead of the compact tile list; 64: never the two-tile CTA-pair kernel at
     head dim 128; 128: the two-tile CTA-pair kernel (two query tiles per CTA,
@@ -368,9 +368,10 @@ def sdp_fwd_noalloc_ptr(q: int, k: int, v: int, o: int, lse: int, B: int, Hq: in
     outputs), but the library allocates no device memory for it: for callers
     whose device memory is owned entirely by their own pool or host
     application and that therefore cannot let a library call cudaMalloc. Its
-    status word lives in a 256-byte array inside the library shared by all
-    such calls, so overlapping calls on different unordered streams race on
-    it; read it with noalloc_status(), not poll_status().
+    status word (and the persistent kernel's claim counters) live in a static
+    array inside the library shared by all such calls, so overlapping calls on
+    different unordered streams race on the status word; read it with
+    noalloc_status(), not poll_status().
     """
     L = lib()
     fn = L.sdp_fwd_noalloc

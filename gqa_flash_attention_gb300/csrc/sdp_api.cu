@@ -26,6 +26,8 @@ std::atomic<int> g_last_cuda_error{0};
 std::atomic<unsigned> g_timeout_ms{kDefaultTimeoutMs};
 std::atomic<int> g_debug_flags{0};
 std::atomic<unsigned> g_last_detail{0};
+// Round-robin index of the claim counter a launch gets (after its device's status word).
+std::atomic<unsigned> g_claim_next{0};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -94,10 +96,12 @@ int device_state(int dev, unsigned int **status, cudaStream_t)
     if (rc != SDP_OK)
         return rc;
     if (g_status[dev] == nullptr) {
+        // the status word, then the claim counters of the persistent single-CTA kernel
+        const size_t bytes = (1 + sdp::CLAIM_SLOTS) * sizeof(unsigned int);
         unsigned int *p = nullptr;
-        cudaError_t e = cudaMalloc(&p, sizeof(unsigned int));
+        cudaError_t e = cudaMalloc(&p, bytes);
         if (e == cudaSuccess)
-            e = cudaMemset(p, 0, sizeof(unsigned int));
+            e = cudaMemset(p, 0, bytes);
         if (e != cudaSuccess) {
             if (p)
                 cudaFree(p);
@@ -346,8 +350,9 @@ int launch(const Shape &sh, const void *q, const void *k, const void *v, void *o
     p.kv_splits = sh.splits;
     p.tiles_per_split = sh.tiles_per_split;
     p.planes_q = static_cast<int>(sh.planes_q);
-    p.o = o;  // [planes, Sq, D]: the persistent CTA-pair kernel writes O rows directly
+    p.o = o;  // [planes, Sq, D]: the persistent kernels write O rows directly
     p.num_sms = sms;
+    p.claim = status + 1 + g_claim_next.fetch_add(1u, std::memory_order_relaxed) % sdp::CLAIM_SLOTS;
 
     const int grid = static_cast<int>(sh.units * sh.splits);
     cudaError_t e;
@@ -642,7 +647,7 @@ const char *sdp_strerror(int code)
     }
 }
 
-int sdp_version(void) { return 105; }
+int sdp_version(void) { return 106; }
 
 void sdp_shutdown(void)
 {

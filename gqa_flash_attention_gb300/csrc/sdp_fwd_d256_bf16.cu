@@ -1,5 +1,6 @@
 // Instantiation of the attention forward kernels: head dim 256, bf16 I/O.
 #include "sdp_fwd_pair_persist.cuh"
+#include "sdp_fwd_persist.cuh"
 #include "sdp_launch.h"
 
 namespace sdp {
@@ -11,6 +12,8 @@ cudaError_t launch_d256_bf16(const LaunchMaps &m, const KernelParams &p, int gri
             return launch_sdp_fwd_pair_persistent<256, true>(m.q, m.k_half, m.v, p, grid, stream);
         return launch_sdp_fwd_pair<256, true>(m.q, m.k_half, m.v, m.o, p, grid, stream);
     }
+    if (use_persist(p, grid))
+        return launch_sdp_fwd_persist<256, true>(m.q, m.k, m.v, p, grid, stream);
     return launch_sdp_fwd<256, true>(m.q, m.k, m.v, m.o, p, grid, stream);
 }
 

@@ -39,9 +39,17 @@ struct KernelParams {
     // SM count, cached per device so that a launch makes no attribute query.
     int num_sms;
     // Units of the launch (the per-unit grid: one CTA per unit); set by the
-    // persistent launcher, whose grid is smaller.
+    // persistent launchers, whose grids are smaller.
     int units;
+    // A counter for the persistent single-CTA kernel's unit claims: one word of the
+    // launching device's status region (the status word, then CLAIM_SLOTS counters),
+    // taken round robin per launch so that launches in flight on different streams
+    // use different words; zeroed in stream order by the launcher that uses it.
+    unsigned int *claim;
 };
+
+// Claim counters after the status word of each device's status region.
+constexpr int CLAIM_SLOTS = 1024;
 
 // Sequences per batch up to which causal variable-length launches use the compact
 // unit list (its level-order search holds two sequences per lane in registers).

@@ -25,10 +25,11 @@
 namespace {
 
 // Scratch shared by every sdp_fwd_noalloc call in the process. Word 0 is the
-// kernel's status word; the rest is headroom up to the stated maximum.
+// kernel's status word, then the claim counters of the persistent single-CTA
+// kernel (the same layout as sdp_fwd's per-device status region).
 constexpr unsigned kScratchWords = SDP_NOALLOC_SCRATCH_BYTES / sizeof(unsigned int);
 constexpr unsigned kStatusWordsPerCall = 1;
-static_assert(kStatusWordsPerCall <= kScratchWords, "scratch array too small for one call");
+static_assert(1 + sdp::CLAIM_SLOTS <= kScratchWords, "scratch array too small for the status region");
 
 static __device__ __align__(256) unsigned int g_noalloc_scratch[kScratchWords];
 

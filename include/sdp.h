@@ -196,11 +196,14 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
  * Arguments, layout, ownership, validation and results are those of sdp_fwd,
  * and the launch is sdp_fwd's own: the same head packing, the same kernel
  * choice, the same wait limit (sdp_set_wait_timeout_ms) and debug flags, so the
- * outputs are bit for bit those of sdp_fwd. The kernel's only scratch, its
- * status word, lives in a static device array of SDP_NOALLOC_SCRATCH_BYTES
- * inside the library, which every GPU that loads the library holds until the
- * process exits. A launch needs 4 bytes of it whatever the problem size; a
- * call needing more than the array holds would return SDP_ERR_OVERFLOW.
+ * outputs are bit for bit those of sdp_fwd. The kernels' only scratch, the
+ * status word and the unit-claim counters of the persistent single-CTA kernel
+ * (1024 words, one per launch round robin, zeroed in stream order by the
+ * launches that use them), lives in a static device array of
+ * SDP_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
+ * library holds until the process exits; sdp_fwd keeps the same region in its
+ * per-device allocation. A launch needs 4 bytes of it for the status word
+ * whatever the problem size.
  *
  * Set-up: the first call on each device (made with that device current)
  * looks up the device address of the array with cudaGetSymbolAddress and
@@ -214,7 +217,7 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
  * tile unwritten and records the event in that word, not in the word that
  * sdp_poll_status reads: read it with sdp_fwd_noalloc_status.
  */
-#define SDP_NOALLOC_SCRATCH_BYTES 256
+#define SDP_NOALLOC_SCRATCH_BYTES 4352
 int sdp_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
                     int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale, int dtype,
                     void *stream);
@@ -260,9 +263,9 @@ unsigned int sdp_set_wait_timeout_ms(unsigned int ms);
  * the same result; tests compare them). Bit 2: never pack the query heads of
  * a group into one head (same result; tests compare). Bit 3: at head dim 128,
  * use the CTA-pair kernel where it qualifies (by default head dim 128 runs on
- * single CTAs, which measured as fast or faster there). Bit 4: one CTA pair
- * per unit even where the persistent CTA-pair kernel applies (same result, bit
- * for bit). Bit 5: variable-length launches cover the longest sequence's query
+ * single CTAs, which measured as fast or faster there). Bit 4: one CTA (or CTA
+ * pair) per unit even where a persistent kernel applies (same result, bit for
+ * bit). Bit 5: variable-length launches cover the longest sequence's query
  * tiles for every sequence instead of the list of tiles that exist (same
  * result, bit for bit). Bit 6: at head dim 128, never the two-tile CTA-pair
  * kernel. Bit 7: at head dim 128, run dense non-causal launches whose two-tile
@@ -279,7 +282,8 @@ int sdp_last_cuda_error(void);
 const char *sdp_strerror(int code);
 
 /* ABI version: 100 * major + minor (101: sdp_fwd_causal; 102: sdp_merge; 103: split-KV; 104: varlen;
- * 105: sdp_fwd_noalloc_status). */
+ * 105: sdp_fwd_noalloc_status; 106: SDP_NOALLOC_SCRATCH_BYTES 4352, the status region holds the
+ * persistent single-CTA kernel's claim counters). */
 int sdp_version(void);
 
 /* Free the per-device status words and forget the cached tensor maps (host

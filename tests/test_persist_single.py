@@ -1,0 +1,114 @@
+"""The persistent single-CTA kernel. Dense launches that run on single CTAs
+(head dim 128; an odd group size under the causal mask; debug flag 2) with more
+units than SMs run one CTA per SM, each claiming units in launch order from a
+per-launch counter. Checked here: every row against the oracle (units of
+different lengths under the causal mask, ragged tiles, packed heads, an odd
+group size at head dim 256), bit-equality with the per-unit launch (debug flag
+16: each unit's arithmetic does not depend on which CTA runs it), launches in
+flight on two streams at once (different claim counters), and graph replay."""
+import pytest
+import torch
+
+import gqa_flash_attention_gb300 as sdp
+from gqa_flash_attention_gb300 import workloads
+from gqa_flash_attention_gb300.workloads import Workload
+from test_parity import check_full
+
+pytestmark = pytest.mark.gpu
+
+DEBUG_SINGLE_CTA = 2
+DEBUG_NO_PERSIST = 16
+
+CASES = [
+    # 160 units of six KV tiles, the last ragged
+    Workload("ps_d128_fp16", 1, 8, 2, 2560, 700, 128, "fp16", seed=301),
+    # 160 causal units of 1 to 20 KV tiles
+    Workload("ps_d128_bf16_causal", 1, 8, 2, 2560, 2560, 128, "bf16", seed=302, causal=True),
+    # MHA, more query rows than keys: 192 causal units, the late ones all read the three KV tiles
+    Workload("ps_d128_mha_sq_gt_skv", 2, 12, 12, 1000, 300, 128, "fp16", seed=303, causal=True),
+    # three query heads per KV head under the causal mask: no CTA pairs at head dim 256, 168 units
+    Workload("ps_d256_g3_causal", 1, 6, 2, 3500, 1000, 256, "bf16", seed=304, causal=True),
+    # Sq not a multiple of 128: eight heads packed into 2400 rows per KV head, 190 units
+    Workload("ps_d128_packed", 5, 16, 2, 300, 900, 128, "fp16", seed=305),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gqa_flash_attention_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+    sdp.lib()
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_persistent_single_cta_every_row(w):
+    check_full(w)
+
+
+def _run(w, flags=0, stream=None):
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    old = sdp.set_debug_flags(flags)
+    try:
+        o, lse = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=w.causal, stream=stream)
+        assert sdp.poll_status() == sdp.SDP_OK
+    finally:
+        sdp.set_debug_flags(old)
+    return o, lse
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_persistent_single_cta_matches_the_per_unit_launch_bit_for_bit(w):
+    o1, l1 = _run(w)
+    o2, l2 = _run(w, DEBUG_NO_PERSIST)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_forced_single_cta_at_d256_runs_persistent_and_matches_per_unit():
+    """Debug flag 2 (single CTAs) on a dense D=256 launch of 160 units: the persistent single-CTA
+    kernel, bit for bit the per-unit single-CTA launch."""
+    w = Workload("ps_d256_forced", 1, 8, 2, 2560, 500, 256, "fp16", seed=306)
+    o1, l1 = _run(w, DEBUG_SINGLE_CTA)
+    o2, l2 = _run(w, DEBUG_SINGLE_CTA | DEBUG_NO_PERSIST)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_two_streams_at_once_take_different_claim_counters():
+    """Two persistent launches in flight together on unordered streams must not share a counter."""
+    wa, wb = CASES[0], CASES[1]
+    ref_a, ref_b = _run(wa), _run(wb)
+    qa, ka, va = (t.cuda() for t in workloads.make_inputs(wa))
+    qb, kb, vb = (t.cuda() for t in workloads.make_inputs(wb))
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    torch.cuda.synchronize()
+    for _ in range(4):
+        with torch.cuda.stream(sa):
+            oa = sdp.sdp_fwd(qa, ka, va, scale=wa.softmax_scale, causal=wa.causal)
+        with torch.cuda.stream(sb):
+            ob = sdp.sdp_fwd(qb, kb, vb, scale=wb.softmax_scale, causal=wb.causal)
+        outs.append((oa, ob))
+    torch.cuda.synchronize()
+    assert sdp.poll_status() == sdp.SDP_OK
+    for (o_a, l_a), (o_b, l_b) in outs:
+        assert torch.equal(o_a, ref_a[0]) and torch.equal(l_a, ref_a[1])
+        assert torch.equal(o_b, ref_b[0]) and torch.equal(l_b, ref_b[1])
+
+
+def test_persistent_single_cta_replays_from_a_cuda_graph():
+    w = CASES[1]
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    o_eager, l_eager = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=True)
+    o = torch.empty_like(q)
+    lse = torch.empty_like(l_eager)
+    sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=True, out=o, lse=lse)  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=True, out=o, lse=lse)
+    o.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert sdp.poll_status() == sdp.SDP_OK
+    assert torch.equal(o, o_eager) and torch.equal(lse, l_eager)

@@ -37,7 +37,9 @@ def _built():
     (DEBUG_NO_LOADS | 128, Workload("timeout_pair2", 1, 4, 2, 256, 384, 128, "bf16", seed=93)),
     # 160 causal units of a dense D=256 launch: the persistent CTA-pair kernel's causal walk
     (DEBUG_NO_LOADS, Workload("timeout_persist_causal", 1, 8, 2, 2560, 2560, 256, "fp16", seed=94, causal=True)),
-], ids=["cta_pair", "single_cta", "persistent_pair", "two_tile_pair", "persistent_causal"])
+    # 160 units of a dense D=128 launch: the persistent single-CTA kernel (no unit is ever announced)
+    (DEBUG_NO_LOADS, Workload("timeout_persist_single", 1, 8, 2, 2560, 384, 128, "fp16", seed=97)),
+], ids=["cta_pair", "single_cta", "persistent_pair", "two_tile_pair", "persistent_causal", "persistent_single"])
 def test_wait_timeout_is_reported_and_the_context_survives(flags, w):
     q, k, v = (t.cuda() for t in workloads.make_inputs(w))
     assert sdp.poll_status() == sdp.SDP_OK

@@ -85,6 +85,8 @@ def test_two_calls_in_a_row_match_sdp_fwd():
 @pytest.mark.parametrize("w", [
     # 160 units of a dense D=256 launch: sdp_fwd runs the persistent CTA-pair kernel here
     Workload("noalloc_persistent", 1, 8, 2, 2560, 384, 256, "fp16", seed=53),
+    # 160 units of a dense D=128 launch: the persistent single-CTA kernel and its claim counter
+    Workload("noalloc_persist_single", 1, 8, 2, 2560, 384, 128, "fp16", seed=56),
     # decode: one query row, 16 heads per KV head, packed into one 16-row tile
     Workload("noalloc_decode", 1, 16, 1, 1, 1000, 256, "fp16", seed=54),
     Workload("noalloc_decode_bf16", 2, 8, 2, 3, 777, 128, "bf16", seed=55),
