@@ -417,13 +417,19 @@ def kernel_name(w, debug_flags=0):
                 name = "sdp_fwd_pair2_kernel"
         if getattr(w, "kv_splits", 1) != 1:
             return name + " + merge_kernel"
-        if name == "sdp_fwd_kernel" and not is_varlen(w) and not debug_flags & 16:
+        if name == "sdp_fwd_kernel" and not is_varlen(w) and not w.causal and not debug_flags & 16:
             sq, G = launch_shape(w)
             if w.B * w.Hkv * G * ((sq + 127) // 128) > sms:
                 return "sdp_fwd_persist_kernel"
         return name
     if is_varlen(w):
-        return "sdp_fwd_pair_kernel" if (w.Hq // w.Hkv) % 2 == 0 else "sdp_fwd_kernel"
+        if (w.Hq // w.Hkv) % 2:
+            return "sdp_fwd_kernel"
+        # causal batches with more (compact-list) units than SMs run the persistent CTA pair
+        n_units = w.Hq * sum((lq + 127) // 128 for lq in w.lens_q)
+        if w.causal and n_units > sms and not debug_flags & 16:
+            return "sdp_fwd_pair_persistent_kernel"
+        return "sdp_fwd_pair_kernel"
     sq, G = launch_shape(w)
     n_qtiles = (sq + 127) // 128
     pair = (n_qtiles * G) % 2 == 0 and not (w.causal and G % 2)
@@ -432,7 +438,7 @@ def kernel_name(w, debug_flags=0):
         return name + " + merge_kernel"
     # dense launches with more units than SMs run the persistent forms
     units = w.B * w.Hkv * G * n_qtiles
-    if units > sms and not debug_flags & 16:
+    if units > sms and not debug_flags & 16 and (pair or not w.causal):
         return "sdp_fwd_pair_persistent_kernel" if pair else "sdp_fwd_persist_kernel"
     return name
 

@@ -1,11 +1,13 @@
 // Persistent form of the single-CTA kernel (see sdp_fwd_kernel.cuh), for dense
-// launches (no variable-length batch, no split-KV) with more units than SMs:
+// launches (no variable-length batch, no split-KV; the launcher keeps causal
+// launches on the per-unit grid) with more units than SMs:
 // one CTA per SM runs unit after unit, with no set-up or tear-down between
 // them, and the next unit starts while the current one ends.
 //
 // Units are claimed in launch order: CTA c first takes unit c, then each CTA
-// takes gridDim + atomicAdd(counter, 1) whenever it starts a unit (the counter
-// is zeroed in stream order before the launch). A static walk (c, c + C, ...)
+// takes gridDim + atomicAdd(counter, 1) once the loads of its current unit are
+// issued, shortly before it is free (the counter is zeroed in stream order
+// before the launch). A static walk (c, c + C, ...)
 // lets CTAs drift apart over the rounds, so the units in flight spread over
 // more KV heads than L2 holds; claiming in order keeps them a window of
 // consecutive units, as the hardware's block scheduler does for the per-unit
@@ -205,11 +207,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (done)
                     break;
                 const Unit un = unit_of(u);
-                // the next unit's claim now, so that its latency passes while this unit loads
-                int next = 0;
-                if (lane == 0)
-                    next = static_cast<int>(gridDim.x) + static_cast<int>(atomicAdd(p.claim, 1u));
-                next = __shfl_sync(0xffffffffu, next, 0);
                 ptx::mbar_arrive_expect_tx_w(q_full0 + 8u * b, L::Q_BYTES);
 #pragma unroll
                 for (int c = 0; c < D / L::BOX_COLS; ++c)
@@ -242,7 +239,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (ok)
                         ok = load_tile(&tm_v, j);
                 }
-                u = next;
+                // The next unit is claimed only now, with this unit's loads issued (the ring keeps the
+                // producer a few tiles ahead of the MMAs): a CTA takes a unit when it is about to be
+                // free, as the block scheduler hands out the per-unit grid. Claiming a whole unit ahead
+                // left long causal units queued behind busy CTAs at the end (-12 % on causal MHA).
+                int next = 0;
+                if (lane == 0)
+                    next = static_cast<int>(gridDim.x) + static_cast<int>(atomicAdd(p.claim, 1u));
+                u = __shfl_sync(0xffffffffu, next, 0);
             }
         }
     } else if (warp == 5) {
@@ -566,14 +570,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-// Dense launches (no variable-length batch, no split-KV, an O pointer for the row-wise
-// stores, a claim counter) with more units than SMs.
+// Dense launches without the causal mask (no variable-length batch, no split-KV, an O
+// pointer for the row-wise stores, a claim counter) with more units than SMs. Under the
+// mask the per-unit grid measured faster (causal MHA at D=128: -1.5 to -1.8 % for this
+// kernel even with late claims): its units' lengths differ, and the block scheduler evens
+// out their end better.
 inline bool use_persist(const KernelParams &p, int grid)
 {
     if (p.debug_flags & DEBUG_NO_PERSIST)
         return false;
-    return p.kv_splits == 1 && p.cu_q == nullptr && p.o != nullptr && p.claim != nullptr && p.num_sms > 0 &&
-           grid > p.num_sms;
+    return !p.causal && p.kv_splits == 1 && p.cu_q == nullptr && p.o != nullptr && p.claim != nullptr &&
+           p.num_sms > 0 && grid > p.num_sms;
 }
 
 // Host-side launcher: one CTA per SM (the units are claimed inside).

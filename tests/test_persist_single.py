@@ -1,11 +1,12 @@
-"""The persistent single-CTA kernel. Dense launches that run on single CTAs
-(head dim 128; an odd group size under the causal mask; debug flag 2) with more
-units than SMs run one CTA per SM, each claiming units in launch order from a
-per-launch counter. Checked here: every row against the oracle (units of
-different lengths under the causal mask, ragged tiles, packed heads, an odd
-group size at head dim 256), bit-equality with the per-unit launch (debug flag
-16: each unit's arithmetic does not depend on which CTA runs it), launches in
-flight on two streams at once (different claim counters), and graph replay."""
+"""The persistent single-CTA kernel. Dense launches without the causal mask
+that run on single CTAs (head dim 128; an odd group size whose units do not
+pair; debug flag 2) with more units than SMs run one CTA per SM, each claiming
+units in launch order from a per-launch counter. Checked here: every row
+against the oracle (ragged tiles, MHA, odd group sizes, packed heads, head dim
+256), bit-equality with the per-unit launch (debug flag 16: each unit's
+arithmetic does not depend on which CTA runs it), launches in flight on two
+streams at once (different claim counters), and graph replay. Causal launches
+keep the per-unit grid (they are covered by the parity suite)."""
 import pytest
 import torch
 
@@ -22,12 +23,12 @@ DEBUG_NO_PERSIST = 16
 CASES = [
     # 160 units of six KV tiles, the last ragged
     Workload("ps_d128_fp16", 1, 8, 2, 2560, 700, 128, "fp16", seed=301),
-    # 160 causal units of 1 to 20 KV tiles
-    Workload("ps_d128_bf16_causal", 1, 8, 2, 2560, 2560, 128, "bf16", seed=302, causal=True),
-    # MHA, more query rows than keys: 192 causal units, the late ones all read the three KV tiles
-    Workload("ps_d128_mha_sq_gt_skv", 2, 12, 12, 1000, 300, 128, "fp16", seed=303, causal=True),
-    # three query heads per KV head under the causal mask: no CTA pairs at head dim 256, 168 units
-    Workload("ps_d256_g3_causal", 1, 6, 2, 3500, 1000, 256, "bf16", seed=304, causal=True),
+    # MHA, bf16: 192 units of three KV tiles, ragged query tile
+    Workload("ps_d128_mha_bf16", 2, 12, 12, 1000, 300, 128, "bf16", seed=302),
+    # three query heads per KV head: 168 units
+    Workload("ps_d128_g3", 1, 12, 4, 1700, 900, 128, "fp16", seed=303),
+    # head dim 256, three heads per KV head over 21 query tiles: units that do not pair, 189 of them
+    Workload("ps_d256_g3", 1, 9, 3, 2600, 700, 256, "bf16", seed=304),
     # Sq not a multiple of 128: eight heads packed into 2400 rows per KV head, 190 units
     Workload("ps_d128_packed", 5, 16, 2, 300, 900, 128, "fp16", seed=305),
 ]
@@ -98,14 +99,14 @@ def test_two_streams_at_once_take_different_claim_counters():
 def test_persistent_single_cta_replays_from_a_cuda_graph():
     w = CASES[1]
     q, k, v = (t.cuda() for t in workloads.make_inputs(w))
-    o_eager, l_eager = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=True)
+    o_eager, l_eager = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale)
     o = torch.empty_like(q)
     lse = torch.empty_like(l_eager)
-    sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=True, out=o, lse=lse)  # warm-up outside capture
+    sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse)  # warm-up outside capture
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, causal=True, out=o, lse=lse)
+        sdp.sdp_fwd(q, k, v, scale=w.softmax_scale, out=o, lse=lse)
     o.zero_()
     for _ in range(3):
         g.replay()
