@@ -402,7 +402,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int lane = threadIdx.x & 31;
 
     // Unit order: head-in-group fastest, then query tile, then (batch, KV head),
-    // so CTAs resident together read the same K/V tiles from L2.
+    // so CTAs resident together read the same K/V tiles from L2 (dense causal
+    // launches: query tile outside a block of KV groups, below).
     int u = blockIdx.x;
     // KV split (split-KV launches): the outermost unit coordinate.
     const int units_per_split = static_cast<int>(gridDim.x) / p.kv_splits;
@@ -423,9 +424,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int n_bg = VARLEN ? p.nseq * p.Hkv : units_per_split / (p.G * p.n_qtiles);
         qt = p.n_qtiles - 1 - u / n_bg;
         bg = u % n_bg;
+    } else if (p.causal) {
+        // Causal units do qt + 1 tiles. Blocks of W consecutive KV groups (at least
+        // CAUSAL_LANES heads), longest tiles first inside a block across its groups: the
+        // grid's last units are short ones of several heads rather than one head's whole
+        // range of lengths, and the units in flight read at most a block's K/V.
+        const int n_bg = units_per_split / (p.G * p.n_qtiles);
+        const int W = min(n_bg, (CAUSAL_LANES + p.G - 1) / p.G);
+        const int blk = u / (W * p.n_qtiles);
+        const int r = u - blk * W * p.n_qtiles;
+        const int wsz = min(W, n_bg - blk * W);
+        qt = p.n_qtiles - 1 - r / wsz;
+        bg = blk * W + r % wsz;
     } else {
-        // Causal units do qt + 1 tiles: start the longest ones first.
-        qt = p.causal ? p.n_qtiles - 1 - (u % p.n_qtiles) : (u % p.n_qtiles);
+        qt = u % p.n_qtiles;
         bg = u / p.n_qtiles;
     }
     const int b = bg / p.Hkv;

@@ -51,6 +51,10 @@ struct KernelParams {
 // Claim counters after the status word of each device's status region.
 constexpr int CLAIM_SLOTS = 1024;
 
+// Heads per block of the dense causal single-CTA unit order: query tiles go longest
+// first across the heads of a block of ceil(CAUSAL_LANES / G) KV groups.
+constexpr int CAUSAL_LANES = 4;
+
 // Sequences per batch up to which causal variable-length launches use the compact
 // unit list (its level-order search holds two sequences per lane in registers).
 constexpr int VARLEN_LEVEL_MAX_SEQS = 64;

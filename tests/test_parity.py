@@ -206,6 +206,36 @@ def test_causal_single_cta_kernel_every_row(w):
         sdp.set_debug_flags(old)
 
 
+# Dense causal single-CTA launches order their units by query tile (longest first) inside blocks of
+# ceil(4 / G) KV groups; these shapes leave a partial last block or a single short one.
+CAUSAL_BLOCKS = [
+    # MHA, five heads: blocks of four KV groups and of one; six query tiles, the last ragged
+    Workload("causal_blk_mha5_d128_fp16", 1, 5, 5, 700, 700, 128, "fp16", seed=76, causal=True),
+    # three heads per group (blocks of two groups), two batches, fewer queries than keys
+    Workload("causal_blk_g3_b2_d128_bf16", 2, 6, 2, 450, 500, 128, "bf16", seed=77, causal=True),
+    # three KV groups, fewer than a block
+    Workload("causal_blk_mha_b3_d128_bf16", 3, 1, 1, 600, 600, 128, "bf16", seed=78, causal=True),
+    # two heads per group, seven groups: blocks of two, two, two and one
+    Workload("causal_blk_g2_d128_fp16", 1, 14, 7, 300, 300, 128, "fp16", seed=79, causal=True),
+    # more queries than keys: the last query tiles see every key
+    Workload("causal_blk_mha6_d128_bf16", 1, 6, 6, 520, 260, 128, "bf16", seed=80, causal=True),
+]
+
+
+@pytest.mark.parametrize("w", CAUSAL_BLOCKS, ids=lambda w: w.name)
+def test_causal_unit_blocks_every_row(w):
+    check_full(w)
+
+
+def test_causal_unit_blocks_single_cta_at_d256_every_row():
+    """Debug flag 2 at head dim 256, five MHA heads: the same block order on the single-CTA kernel."""
+    old = sdp.set_debug_flags(DEBUG_SINGLE_CTA)
+    try:
+        check_full(Workload("causal_blk_mha5_d256_fp16", 1, 5, 5, 400, 400, 256, "fp16", seed=81, causal=True))
+    finally:
+        sdp.set_debug_flags(old)
+
+
 
 def test_dense_call_replays_from_a_cuda_graph():
     w = workloads.WORKLOADS["gqa4_s256_d128_fp16"]
