@@ -349,6 +349,21 @@ __device__ __forceinline__ int varlen_compact_unit(const KernelParams &p, int u)
     return p.causal ? (p.n_qtiles - 1 - r.qt) * (p.nseq * p.Hkv) + bg : bg * p.n_qtiles + r.qt;
 }
 
+// Dense causal launches: query tile qt and (batch, KV head) bg of unit u (head-in-group
+// index already taken out; n_bg = B * Hkv). A unit does qt + 1 tiles. Blocks of W
+// consecutive KV groups (at least CAUSAL_LANES heads), longest tiles first inside a block
+// across its groups: the grid's last units are short ones of several heads rather than one
+// head's whole range of lengths, and the units in flight read at most a block's K/V.
+__device__ __forceinline__ void causal_block_unit(const KernelParams &p, int u, int n_bg, int &qt, int &bg)
+{
+    const int W = min(n_bg, (CAUSAL_LANES + p.G - 1) / p.G);
+    const int blk = u / (W * p.n_qtiles);
+    const int r = u - blk * W * p.n_qtiles;
+    const int wsz = min(W, n_bg - blk * W);
+    qt = p.n_qtiles - 1 - r / wsz;
+    bg = blk * W + r % wsz;
+}
+
 // Position of a chunk in the load order K_0, then for j = 0..n-1: K_{j+1} (if
 // any), V_j. Tiles are CPT chunks long; the producer and both issuers derive
 // ring slot = pos % NSLOTS and phase = (pos / NSLOTS) & 1 from it. Every
@@ -425,17 +440,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         qt = p.n_qtiles - 1 - u / n_bg;
         bg = u % n_bg;
     } else if (p.causal) {
-        // Causal units do qt + 1 tiles. Blocks of W consecutive KV groups (at least
-        // CAUSAL_LANES heads), longest tiles first inside a block across its groups: the
-        // grid's last units are short ones of several heads rather than one head's whole
-        // range of lengths, and the units in flight read at most a block's K/V.
-        const int n_bg = units_per_split / (p.G * p.n_qtiles);
-        const int W = min(n_bg, (CAUSAL_LANES + p.G - 1) / p.G);
-        const int blk = u / (W * p.n_qtiles);
-        const int r = u - blk * W * p.n_qtiles;
-        const int wsz = min(W, n_bg - blk * W);
-        qt = p.n_qtiles - 1 - r / wsz;
-        bg = blk * W + r % wsz;
+        causal_block_unit(p, u, units_per_split / (p.G * p.n_qtiles), qt, bg);
     } else {
         qt = u % p.n_qtiles;
         bg = u / p.n_qtiles;
