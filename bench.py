@@ -397,13 +397,14 @@ def launch_shape(w):
     return w.Sq, G
 
 
-def kernel_name(w, debug_flags=0):
+def kernel_name(w, debug_flags=0, captured=False):
     """The kernel sdp_fwd launches for this workload: the CTA-pair kernel when
     the units of each (batch, KV head) pair up (and, causal, share the query
     tile), else the single-CTA kernel, each in its persistent form for dense
     launches with more units than SMs (debug bit 4 keeps one CTA or pair per
-    unit); split-KV adds the merge kernel; variable-length batches pair up when
-    the group size is even; head dim 128 runs on single CTAs."""
+    unit; a launch captured into a graph keeps one CTA per unit on single CTAs);
+    split-KV adds the merge kernel; variable-length batches pair up when the
+    group size is even; head dim 128 runs on single CTAs."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
     if w.D == 128:
         # dense, non-causal launches whose two-tile units pair up and fill a wave of CTAs run the
@@ -417,7 +418,7 @@ def kernel_name(w, debug_flags=0):
                 name = "sdp_fwd_pair2_kernel"
         if getattr(w, "kv_splits", 1) != 1:
             return name + " + merge_kernel"
-        if name == "sdp_fwd_kernel" and not is_varlen(w) and not w.causal and not debug_flags & 16:
+        if name == "sdp_fwd_kernel" and not is_varlen(w) and not w.causal and not debug_flags & 16 and not captured:
             sq, G = launch_shape(w)
             if w.B * w.Hkv * G * ((sq + 127) // 128) > sms:
                 return "sdp_fwd_persist_kernel"
@@ -439,7 +440,10 @@ def kernel_name(w, debug_flags=0):
     # dense launches with more units than SMs run the persistent forms
     units = w.B * w.Hkv * G * n_qtiles
     if units > sms and not debug_flags & 16 and (pair or not w.causal):
-        return "sdp_fwd_pair_persistent_kernel" if pair else "sdp_fwd_persist_kernel"
+        if pair:
+            return "sdp_fwd_pair_persistent_kernel"
+        if not captured:
+            return "sdp_fwd_persist_kernel"
     return name
 
 
@@ -647,7 +651,7 @@ def ours_arm(args, w):
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
                     "traffic": load_traffic(w.name), "peak_source": f"{hbm_src} HBM copy bandwidth",
                     "algorithmic_bytes": w.hbm_bytes(), "tflops": tflops}
-    roofline.update({"kernel": kernel_name(w, args.debug_flags), "launch_ms_median": statistics.median(per_launch_ms),
+    roofline.update({"kernel": kernel_name(w, args.debug_flags, use_graph), "launch_ms_median": statistics.median(per_launch_ms),
                      "flop_per_byte": intensity})
     if roofline["bound"] == "tensor":
         roofline.update({"peak_datasheet": DATASHEET_TFLOPS, "frac_datasheet": tflops / DATASHEET_TFLOPS,

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <initializer_list>
 #include <mutex>
+#include <unordered_map>
 
 #include "sdp.h"
 #include "sdp_launch.h"
@@ -26,8 +27,12 @@ std::atomic<int> g_last_cuda_error{0};
 std::atomic<unsigned> g_timeout_ms{kDefaultTimeoutMs};
 std::atomic<int> g_debug_flags{0};
 std::atomic<unsigned> g_last_detail{0};
-// Round-robin index of the claim counter a launch gets (after its device's status word).
-std::atomic<unsigned> g_claim_next{0};
+// Claim counters of the persistent single-CTA kernel (after each device's status word): one
+// per stream, found by the stream's unique id, so that only launches ordered on one stream
+// share a counter (each zeroes it in stream order before its kernel). g_claim_mu is held
+// across the reset and the launch, so two host threads on one stream cannot interleave them.
+std::mutex g_claim_mu;
+std::unordered_map<unsigned long long, int> g_claim_slot;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -115,6 +120,22 @@ int device_state(int dev, unsigned int **status, cudaStream_t)
 
 // 3-D map over a [planes, rows, D] 16-bit tensor; box = 64 columns x box_rows rows
 // x 1 plane with 128-byte swizzle. Rows past `rows` read as zero and are not written.
+// The encoder is a driver entry point and needs a current context. A host thread that has
+// made no runtime call yet has none (the runtime binds the device's primary context to a
+// thread lazily, on its first call that needs it), so on CUDA_ERROR_INVALID_CONTEXT the
+// current device's primary context is bound (cudaSetDevice) and the encode retried once.
+template <class Encode>
+CUresult encode_in_context(Encode &&encode)
+{
+    CUresult r = encode();
+    if (r == CUDA_ERROR_INVALID_CONTEXT) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess)
+            r = encode();
+    }
+    return r;
+}
+
 int encode_map_uncached(CUtensorMap *map, const void *base, int dtype, int D, long long rows, long long planes,
                         unsigned box_rows)
 {
@@ -126,10 +147,11 @@ int encode_map_uncached(CUtensorMap *map, const void *base, int dtype, int D, lo
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
     const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estride[3] = {1, 1, 1};
-    CUresult r = enc(map, dtype == SDP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                     const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = encode_in_context([&] {
+        return enc(map, dtype == SDP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    });
     if (r != CUDA_SUCCESS)
         return cuda_fail(cudaErrorInvalidValue);
     return SDP_OK;
@@ -149,10 +171,11 @@ int encode_map_thd_uncached(CUtensorMap *map, const void *base, int dtype, int D
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads) * D * 2, static_cast<cuuint64_t>(D) * 2};
     const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estride[3] = {1, 1, 1};
-    CUresult r = enc(map, dtype == SDP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                     const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = encode_in_context([&] {
+        return enc(map, dtype == SDP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void *>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    });
     if (r != CUDA_SUCCESS)
         return cuda_fail(cudaErrorInvalidValue);
     return SDP_OK;
@@ -316,6 +339,34 @@ long long workspace_bytes(const Shape &sh, int D)
     return align256(sh.splits * rows * D * 2) + sh.splits * rows * 4;
 }
 
+// Claim counter index of stream `st`, or -1 (then no persistent single-CTA launch): the
+// stream is capturing (a graph may be replayed on any stream, beside eager launches that
+// use the same counter), its id cannot be read, or every counter has a stream. The caller
+// holds g_claim_mu.
+int claim_slot_locked(cudaStream_t st)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    if (cs != cudaStreamCaptureStatusNone)
+        return -1;
+    unsigned long long id = 0;
+    if (cudaStreamGetId(st, &id) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    const auto it = g_claim_slot.find(id);
+    if (it != g_claim_slot.end())
+        return it->second;
+    if (g_claim_slot.size() >= static_cast<size_t>(sdp::CLAIM_SLOTS))
+        return -1;
+    const int slot = static_cast<int>(g_claim_slot.size());
+    g_claim_slot.emplace(id, slot);
+    return slot;
+}
+
 // Encode the maps and launch the kernel for `sh`. O / LSE go to `o` / `lse`
 // ([splits * planes_q, Sq, D] and [splits * planes_q, Sq] when splits > 1).
 int launch(const Shape &sh, const void *q, const void *k, const void *v, void *o, float *lse, int Hkv, int Skv,
@@ -352,9 +403,19 @@ int launch(const Shape &sh, const void *q, const void *k, const void *v, void *o
     p.planes_q = static_cast<int>(sh.planes_q);
     p.o = o;  // [planes, Sq, D]: the persistent kernels write O rows directly
     p.num_sms = sms;
-    p.claim = status + 1 + g_claim_next.fetch_add(1u, std::memory_order_relaxed) % sdp::CLAIM_SLOTS;
 
     const int grid = static_cast<int>(sh.units * sh.splits);
+    // A claim counter for launches that may run persistent on single CTAs (dense, unsplit,
+    // unmasked, more units than SMs), held with the lock until the launch is enqueued.
+    std::unique_lock<std::mutex> claim_lk(g_claim_mu, std::defer_lock);
+    if (!causal && sh.splits == 1 && grid > sms) {
+        claim_lk.lock();
+        const int slot = claim_slot_locked(st);
+        if (slot >= 0)
+            p.claim = status + 1 + slot;
+        else
+            claim_lk.unlock();
+    }
     cudaError_t e;
     if (D == 128)
         e = dtype == SDP_BF16 ? sdp::launch_d128_bf16(maps, p, grid, st) : sdp::launch_d128_fp16(maps, p, grid, st);
@@ -647,7 +708,7 @@ const char *sdp_strerror(int code)
     }
 }
 
-int sdp_version(void) { return 106; }
+int sdp_version(void) { return 107; }
 
 void sdp_shutdown(void)
 {
@@ -657,6 +718,10 @@ void sdp_shutdown(void)
             e.valid = false;
     }
     sdp::noalloc_forget();
+    {
+        std::lock_guard<std::mutex> lk(g_claim_mu);
+        g_claim_slot.clear();
+    }
     std::lock_guard<std::mutex> lk(g_mu);
     int cur = 0;
     const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;

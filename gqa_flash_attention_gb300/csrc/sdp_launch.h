@@ -43,8 +43,9 @@ struct KernelParams {
     int units;
     // A counter for the persistent single-CTA kernel's unit claims: one word of the
     // launching device's status region (the status word, then CLAIM_SLOTS counters),
-    // taken round robin per launch so that launches in flight on different streams
-    // use different words; zeroed in stream order by the launcher that uses it.
+    // the launching stream's own, so that only launches ordered on one stream share
+    // it; zeroed in stream order by the launcher that uses it. Null (no persistent
+    // single-CTA launch) under stream capture or when every counter has a stream.
     unsigned int *claim;
 };
 

@@ -60,8 +60,18 @@ extern "C" {
  * Errors: on any validation error nothing is launched and the code is
  * returned. SDP_ERR_CUDA reports a failed tensor-map encode or launch. The
  * call does not synchronise, so a device-side timeout is reported later by
- * sdp_poll_status(). On the first call on a device the library allocates a
- * 4-byte status word there (freed by sdp_shutdown()).
+ * sdp_poll_status(). On the first call on a device the library allocates its
+ * status region there: the status word and 1024 unit-claim counters, 4100
+ * bytes (freed by sdp_shutdown()).
+ *
+ * Streams and graphs: calls on different streams, from any host threads, may
+ * run at once. Launches without the causal mask that run on single CTAs (head
+ * dim 128, or a group size whose units do not pair) with more 128-row units
+ * than SMs use a persistent kernel whose CTAs claim units from a counter of the
+ * launching stream (streams get counters in the order they are first used,
+ * found by the stream's unique id, cudaStreamGetId). A launch captured into a
+ * CUDA graph, or on a stream after the 1024th, runs one CTA per unit instead:
+ * the same results, bit for bit.
  */
 int sdp_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
             int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale, int dtype,
@@ -185,7 +195,7 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
  * The paper has no counterpart: this is a library-usage variant, not a step of
  * the method.
  *
- * sdp_fwd allocates a 4-byte status word on a device the first time it runs
+ * sdp_fwd allocates its 4100-byte status region on a device the first time it runs
  * there (cudaMalloc). Callers that cannot allow that use this entry point
  * instead: code running inside a memory pool or arena that owns all device
  * memory of the process, plugins whose host forbids allocations outside its
@@ -198,7 +208,7 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
  * choice, the same wait limit (sdp_set_wait_timeout_ms) and debug flags, so the
  * outputs are bit for bit those of sdp_fwd. The kernels' only scratch, the
  * status word and the unit-claim counters of the persistent single-CTA kernel
- * (1024 words, one per launch round robin, zeroed in stream order by the
+ * (1024 words, one per stream as for sdp_fwd, zeroed in stream order by the
  * launches that use them), lives in a static device array of
  * SDP_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
  * library holds until the process exits; sdp_fwd keeps the same region in its
@@ -283,7 +293,8 @@ const char *sdp_strerror(int code);
 
 /* ABI version: 100 * major + minor (101: sdp_fwd_causal; 102: sdp_merge; 103: split-KV; 104: varlen;
  * 105: sdp_fwd_noalloc_status; 106: SDP_NOALLOC_SCRATCH_BYTES 4352, the status region holds the
- * persistent single-CTA kernel's claim counters). */
+ * persistent single-CTA kernel's claim counters; 107: one claim counter per stream, captured
+ * launches on the per-unit grid). */
 int sdp_version(void);
 
 /* Free the per-device status words and forget the cached tensor maps (host

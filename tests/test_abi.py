@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_version_and_messages(L):
-    assert L.sdp_version() == 106
+    assert L.sdp_version() == 107
     for code in range(-7, 1):
         assert len(sdp.strerror(code)) > 0
     assert sdp.strerror(-99) == "unknown status code"

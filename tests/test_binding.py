@@ -1,7 +1,9 @@
 """The Python binding's argument checks on a GPU: every malformed call raises
 ValueError before anything is launched, and a well-formed call gives the same
 result with or without caller-provided output buffers, on the current stream
-or on an explicit one."""
+or on an explicit one, and from a host thread whose first CUDA work is the call."""
+import math
+
 import pytest
 import torch
 
@@ -66,3 +68,29 @@ def test_results_do_not_depend_on_buffers_or_stream():
     for o, l in ((o2, l2), (o3, l3), (o4, l4)):
         assert torch.equal(o, o1) and torch.equal(l, l1)
     assert torch.equal(o5, o1)
+
+
+def test_first_call_from_a_fresh_host_thread():
+    """The C call is the first CUDA work of a new host thread, with output buffers whose tensor maps
+    are not cached: the library binds the device's primary context itself (the runtime binds it to a
+    thread only on that thread's first call that needs it)."""
+    import threading
+    q, k, v = tensors()
+    o_ref, l_ref = sdp.sdp_fwd(q, k, v)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((1, 4, 200), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    rc = []
+
+    def worker():
+        rc.append(sdp.sdp_fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                  1, 4, 2, 200, 300, 128, 1.0 / math.sqrt(128), sdp.SDP_FP16, s.cuda_stream))
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    torch.cuda.synchronize()
+    assert rc == [sdp.SDP_OK]
+    assert sdp.poll_status() == sdp.SDP_OK
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)

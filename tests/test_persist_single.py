@@ -5,7 +5,8 @@ units in launch order from a per-launch counter. Checked here: every row
 against the oracle (ragged tiles, MHA, odd group sizes, packed heads, head dim
 256), bit-equality with the per-unit launch (debug flag 16: each unit's
 arithmetic does not depend on which CTA runs it), launches in flight on two
-streams at once (different claim counters), and graph replay. Causal launches
+streams at once (different claim counters), two host threads on one stream (one counter), and
+graph replay (captured launches run the per-unit grid). Causal launches
 keep the per-unit grid (they are covered by the parity suite)."""
 import pytest
 import torch
@@ -96,7 +97,45 @@ def test_two_streams_at_once_take_different_claim_counters():
         assert torch.equal(o_b, ref_b[0]) and torch.equal(l_b, ref_b[1])
 
 
-def test_persistent_single_cta_replays_from_a_cuda_graph():
+def test_two_host_threads_on_one_stream():
+    """Two host threads enqueue persistent launches on the same stream at once. They share the
+    stream's claim counter, so each launch's counter reset and kernel must stay together in
+    stream order."""
+    import threading
+    ws = CASES[0], CASES[1]
+    refs = [_run(w) for w in ws]
+    ins = [tuple(t.cuda() for t in workloads.make_inputs(w)) for w in ws]
+    s = torch.cuda.Stream()
+    outs, errs = [[], []], []
+    torch.cuda.synchronize()
+
+    def worker(i):
+        try:
+            q, k, v = ins[i]
+            with torch.cuda.stream(s):
+                for _ in range(6):
+                    outs[i].append(sdp.sdp_fwd(q, k, v, scale=ws[i].softmax_scale, causal=ws[i].causal))
+        except Exception as e:  # reported below, on the test's thread
+            errs.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errs, errs
+    assert sdp.poll_status() == sdp.SDP_OK
+    for i in range(2):
+        assert len(outs[i]) == 6
+        for o, l in outs[i]:
+            assert torch.equal(o, refs[i][0]) and torch.equal(l, refs[i][1])
+
+
+def test_captured_launch_replays_from_a_cuda_graph():
+    """A launch under stream capture takes no claim counter (a graph may be replayed on any stream,
+    beside eager launches on the capturing stream) and runs the per-unit grid: bit for bit the eager
+    persistent result."""
     w = CASES[1]
     q, k, v = (t.cuda() for t in workloads.make_inputs(w))
     o_eager, l_eager = sdp.sdp_fwd(q, k, v, scale=w.softmax_scale)
