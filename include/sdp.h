@@ -65,7 +65,9 @@ extern "C" {
  * bytes (freed by sdp_shutdown()).
  *
  * Streams and graphs: calls on different streams, from any host threads, may
- * run at once. Launches without the causal mask that run on single CTAs (head
+ * run at once. A host thread's first call may be its first CUDA work: the call
+ * binds the current device's primary context to the thread (cudaSetDevice),
+ * as the runtime itself does on a thread's first call that needs a context. Launches without the causal mask that run on single CTAs (head
  * dim 128, or a group size whose units do not pair) with more 128-row units
  * than SMs use a persistent kernel whose CTAs claim units from a counter of the
  * launching stream (streams get counters in the order they are first used,
