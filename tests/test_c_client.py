@@ -46,6 +46,9 @@ def test_c_client_builds_and_links():
     (Workload("c_splitkv", 2, 16, 2, 1, 3000, 256, "fp16", seed=98), ["splitkv", "0"]),
     (Workload("c_splitkv3", 1, 8, 4, 7, 2000, 128, "bf16", seed=99), ["splitkv", "3"]),
     (Workload("c_noalloc", 1, 16, 1, 1, 1000, 256, "fp16", seed=100), ["noalloc"]),
+    # 160 units at head dim 128: the persistent single-CTA kernel on the legacy default stream
+    (Workload("c_persist", 1, 8, 2, 2560, 500, 128, "fp16", seed=101), ["fwd"]),
+    (Workload("c_persist_noalloc", 1, 8, 2, 2560, 500, 128, "bf16", seed=102), ["noalloc"]),
 ], ids=lambda x: x.name if isinstance(x, Workload) else "-".join(x))
 def test_c_client_matches_the_oracle(w, mode):
     q, k, v = workloads.make_inputs(w)

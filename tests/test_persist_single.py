@@ -152,3 +152,17 @@ def test_captured_launch_replays_from_a_cuda_graph():
     torch.cuda.synchronize()
     assert sdp.poll_status() == sdp.SDP_OK
     assert torch.equal(o, o_eager) and torch.equal(lse, l_eager)
+
+
+def test_calls_after_shutdown_set_up_again():
+    """sdp_shutdown frees the status region and forgets the streams' claim counters; the next call
+    allocates the region again and gives the same result."""
+    w = CASES[0]
+    o1, l1 = _run(w)
+    torch.cuda.synchronize()
+    sdp.lib().sdp_shutdown()
+    o2, l2 = _run(w)
+    o3, l3 = _run(w)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
