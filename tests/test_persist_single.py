@@ -132,6 +132,39 @@ def test_two_host_threads_on_one_stream():
             assert torch.equal(o, refs[i][0]) and torch.equal(l, refs[i][1])
 
 
+def test_per_thread_default_streams_of_two_host_threads():
+    """Two host threads launch on cudaStreamPerThread (handle 2): the same handle names a different
+    stream in each thread, and each stream's unique id gives it its own claim counter."""
+    import threading
+    per_thread_stream = 2
+    ws = CASES[0], CASES[1]
+    refs = [_run(w) for w in ws]
+    ins = [tuple(t.cuda() for t in workloads.make_inputs(w)) for w in ws]
+    outs = [[(torch.empty_like(ins[i][0]), torch.empty_like(refs[i][1])) for _ in range(6)] for i in range(2)]
+    errs = []
+    torch.cuda.synchronize()
+
+    def worker(i):
+        try:
+            q, k, v = ins[i]
+            for o, l in outs[i]:
+                sdp.sdp_fwd(q, k, v, scale=ws[i].softmax_scale, out=o, lse=l, stream=per_thread_stream)
+        except Exception as e:  # reported below, on the test's thread
+            errs.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errs, errs
+    assert sdp.poll_status() == sdp.SDP_OK
+    for i in range(2):
+        for o, l in outs[i]:
+            assert torch.equal(o, refs[i][0]) and torch.equal(l, refs[i][1])
+
+
 def test_captured_launch_replays_from_a_cuda_graph():
     """A launch under stream capture takes no claim counter (a graph may be replayed on any stream,
     beside eager launches on the capturing stream) and runs the per-unit grid: bit for bit the eager
