@@ -194,7 +194,7 @@ int sdp_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *
 
 /*
  * sdp_fwd_noalloc — sdp_fwd for callers that cannot allocate device memory.
- * The paper has no counterpart: this is a library-usage variant, not a step of
+ * No page describes a counterpart: this is a library-usage variant, not a step of
  * the method.
  *
  * sdp_fwd allocates its 4100-byte status region on a device the first time it runs
