@@ -117,13 +117,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         Unit r;
         const int hi = u % p.G;
         u /= p.G;
-        int qt, bg;  // query tile; b * Hkv + g
-        if (p.causal) {
-            causal_block_unit(p, u, p.units / (p.G * p.n_qtiles), qt, bg);
-        } else {
-            qt = u % p.n_qtiles;
-            bg = u / p.n_qtiles;
-        }
+        // Causal launches do not run this kernel (use_persist); the causal order here is the one
+        // its causal measurements used. Decoding the per-unit grid's blocked causal order here
+        // took 219 registers instead of 217 and ran 0.6-1.0 % slower on the dense launches.
+        const int qt = p.causal ? p.n_qtiles - 1 - (u % p.n_qtiles) : (u % p.n_qtiles);
+        const int bg = u / p.n_qtiles;  // b * Hkv + g
         const int b = bg / p.Hkv;
         const int g = bg - b * p.Hkv;
         r.z_q = b * p.Hq + g * p.G + hi;
