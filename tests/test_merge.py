@@ -3,8 +3,6 @@
 I.2), against the oracle merge on the same inputs, and end to end: attention
 over key shards with sdp_fwd, merged with sdp_merge, against the oracle's
 attention over all keys."""
-import math
-
 import numpy as np
 import pytest
 import torch
@@ -13,7 +11,7 @@ import gqa_flash_attention_gb300 as sdp
 import oracle
 from gqa_flash_attention_gb300 import workloads
 from gqa_flash_attention_gb300.workloads import Workload
-from parity import LSE_MAX_ABS, ORACLE_DTYPE, assert_within, compare
+from parity import ORACLE_DTYPE, assert_within, compare
 
 pytestmark = pytest.mark.gpu
 TD = {"fp16": torch.float16, "bf16": torch.bfloat16}
