@@ -62,7 +62,8 @@ extern "C" {
  * call does not synchronise, so a device-side timeout is reported later by
  * sdp_poll_status(). On the first call on a device the library allocates its
  * status region there: the status word and 1024 unit-claim counters, 4100
- * bytes (freed by sdp_shutdown()).
+ * bytes (freed by sdp_shutdown()); the allocation and its zeroing are
+ * synchronous, so make that first call outside stream capture.
  *
  * Streams and graphs: calls on different streams, from any host threads, may
  * run at once. A host thread's first call may be its first CUDA work: the call
